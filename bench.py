@@ -1,0 +1,363 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the nonuniform FFT hot path on GB300.
+
+One step = one type 1 transform (spread -> FFT -> correct) plus one type 2
+transform (correct/pad -> FFT -> interpolate) of the workload's M points,
+each through the C ABI, with the points already bin-sorted (setpts is
+excluded, as in the metric).  value = nonuniform points transformed per
+second over the whole job: 2 M per step per GPU (type 1 + type 2).
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle (the
+three-step NUFFT in double precision, single thread) on a bounded sample of
+the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from nonuniform_fft_gb300 import workloads as W  # noqa: E402
+
+DEFAULT_WORKLOAD = "2d_f32_N1024_M1e7"
+METRIC = "NU points/s (type1 & type2, exec excl. setpts) and % of GB300 HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "nonuniform_fft_gb300", "csrc", f)
+                  for f in ("spreadinterp.cuh", "setpts.cu", "nufft_plan.cu")]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="points per transform in the CPU baseline sample (0: auto)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def algorithmic_bytes(wl: W.Workload, n) -> dict:
+    """Minimum bytes each kernel must move per launch (one transform):
+    coordinates (d reals), one complex strength / result and one 4-byte
+    permutation index per point, plus the fine-grid traffic."""
+    cs = 4 if wl.dtype == "f32" else 8
+    cb = 2 * cs
+    d = wl.dim
+    M = wl.M
+    cells = int(np.prod(n))
+    modes = int(np.prod(wl.N))
+    return {
+        "spread": M * (d * cs + cb + 4) + 2 * cells * cb,   # points in; grid read + written
+        "interp": cells * cb + M * (d * cs + 4 + cb),       # grid in; points in, c out
+        "deconv": 2 * modes * cb,
+        "pad": modes * cb + cells * cb,
+    }
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    try:
+        with open(TRAFFIC_PATH) as fh:
+            t = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in (self.out or "").strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1) -> dict:
+    """Time the oracle's three-step NUFFT (type 1 + type 2) on the first
+    sample_M points of the workload; returns points/s over `steps` repeats."""
+    import oracle
+    sub = wl.scaled(M=sample_M)
+    pts, c = W.sample(sub)
+    fk = W.coefficients(wl)
+    oracle.build()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1])
+        oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2])
+    dt = time.perf_counter() - t0
+    return {"value": 2 * sample_M * steps / dt, "unit": "NU points/s", "cores": 1,
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{sample_M} of {wl.M} points of {wl.name}, full {'x'.join(map(str, wl.N))} "
+                      f"modes, type 1 + type 2, x{steps}; double precision, one thread"}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    # bounded: about a minute of CPU work for the whole --steps + --warmup run
+    per_step = args.cpu_sample or max(20000, int(1.5e6 / max(1, args.steps + args.warmup)))
+    per_step = min(per_step, wl.M)
+    if args.warmup:
+        cpu_oracle_run(wl, min(per_step, 20000), 1)
+    r = cpu_oracle_run(wl, per_step, args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "NU points/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * r["seconds"] / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "N": list(wl.N), "M": wl.M, "eps": wl.eps,
+                   "sample_points_per_transform": per_step},
+        "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": r["value"], "unit": "NU points/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import nonuniform_fft_gb300 as nf
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nf.load_library()
+
+    cname = "complex64" if wl.dtype == "f32" else "complex128"
+    ctorch = getattr(torch, cname)
+    pts, c_np = W.sample(wl)
+    fk_np = W.coefficients(wl)
+    stream = torch.cuda.Stream(dev)
+    N = wl.N
+    with torch.cuda.stream(stream):
+        xs = [torch.from_numpy(p).to(dev) for p in pts]
+        c_in = torch.from_numpy(c_np).to(dev)
+        f_in = torch.from_numpy(fk_np).to(dev)
+        f_out = torch.empty(int(np.prod(N)), dtype=ctorch, device=dev)
+        c_out = torch.empty(wl.M, dtype=ctorch, device=dev)
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream.synchronize()
+    del pts
+
+    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream)
+    p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream)
+    p1.setpts(*xs)
+    p2.setpts(*xs)
+    info = p1.info()
+    n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
+
+    def step():
+        p1.execute(c_in, f_out)
+        p2.execute(c_out, f_in)
+
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage = {k: 0.0 for k in ("spread", "fft1", "deconv", "zero", "pad", "fft2", "interp")}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()                       # evict the inputs from L2 (untimed)
+            ev0[i].record(stream)
+            step()
+            ev1[i].record(stream)
+            t1 = p1.timings()                       # waits for this step's events
+            t2 = p2.timings()
+            stage["spread"] += t1["spread_interp"]
+            stage["fft1"] += t1["fft"]
+            stage["deconv"] += t1["deconv_pad"]
+            stage["zero"] += t1["zero"]
+            stage["pad"] += t2["deconv_pad"]
+            stage["fft2"] += t2["fft"]
+            stage["interp"] += t2["spread_interp"]
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1))
+    t_max = total_ms
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    pts_per_step = 2 * wl.M
+    value = world * pts_per_step * args.steps / (t_max / 1e3)
+
+    # roofline of the dominant kernel (per-launch averages over the timed region)
+    K = args.steps
+    algo = algorithmic_bytes(wl, n)
+    per_launch = {"spread": stage["spread"] / K, "interp": stage["interp"] / K}
+    dom = max(per_launch, key=per_launch.get)
+    with open(PEAKS_PATH) as fh:
+        peaks = json.load(fh)
+    peak = float(peaks["hbm_gbs"])
+    achieved = algo[dom] / (per_launch[dom] / 1e3) / 1e9
+    kernel_name = {"spread": "spread_sm_kernel", "interp": "interp_sm_kernel"}[dom]
+    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak,
+                "traffic": load_traffic(kernel_name, wl.name),
+                "algorithmic_bytes_per_launch": algo[dom], "launch_ms": per_launch[dom],
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured copy bandwidth)"}
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hc = torch.from_numpy(c_np).pin_memory()
+        hf = torch.from_numpy(fk_np).pin_memory()
+        hf_out = torch.empty(int(np.prod(N)), dtype=ctorch).pin_memory()
+        hc_out = torch.empty(wl.M, dtype=ctorch).pin_memory()
+        p1.execute(hc, hf_out)
+        p2.execute(hc_out, hf)
+        e2e_steps = max(3, min(args.steps, 10))
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            p1.execute(hc, hf_out)        # host c in, host f out (synchronous)
+            p2.execute(hc_out, hf)        # host f in, host c out (synchronous)
+        el = time.perf_counter() - t0
+        if world > 1:
+            t = torch.tensor([el], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            el = float(t.item())
+        cb = hc.element_size()
+        modes = int(np.prod(N))
+        e2e = {"value": world * pts_per_step * e2e_steps / el, "unit": "NU points/s",
+               "h2d_bytes_per_step": wl.M * cb + modes * cb,
+               "d2h_bytes_per_step": modes * cb + wl.M * cb}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_run(wl, args.cpu_sample or min(wl.M, 3_000_000), 1)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        steps_ms = total_ms / K
+        line = {
+            "metric": METRIC, "value": value, "unit": "NU points/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": t_max / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "dim": wl.dim, "N": list(wl.N), "M": wl.M,
+                       "eps": wl.eps, "w": info["w"], "fine_grid": n, "dist": wl.dist,
+                       "types": "type 1 (iflag -1) + type 2 (iflag +1) per step",
+                       "points_per_step_per_gpu": pts_per_step,
+                       "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
+                       "msub": info["msub"], "nsub": info["nsub"],
+                       "l2": "flushed between timed steps (256 MiB write, untimed)",
+                       "parallelism": f"replicas x{world}"},
+            "stage_ms_per_step": {k: v / K for k, v in stage.items()},
+            "step_ms_rank0": steps_ms,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 4 * K,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    p1.close()
+    p2.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

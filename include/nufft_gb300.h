@@ -1,0 +1,185 @@
+/*
+ * nufft_gb300.h -- C ABI of the GB300 (sm_103a) nonuniform FFT library.
+ *
+ * Transforms (definitions from "cuFINUFFT: a load-balanced GPU library for
+ * general-purpose nonuniform FFTs", Shih, Wright, Anden, Blaschke, Barnett;
+ * section and equation numbers are that paper's):
+ *
+ *   type 1 (Sec. I eq. (1)):  f_k = sum_{j<M} c_j exp(s i k.x_j),   k in I_N1 x I_N2 (x I_N3)
+ *   type 2 (Sec. I eq. (3)):  c_j = sum_k      f_k exp(s i k.x_j),  j < M
+ *
+ * with s = +1 if iflag >= 0, else -1, I_N = {k integer : -N/2 <= k < N/2}
+ * (eq. (2)), and points x_j in [-pi, pi)^d (any finite value is accepted and
+ * read modulo 2 pi).  They are computed approximately, to relative l2 error
+ * close to eps, by the three-step scheme of Sec. II: spreading with the
+ * "exponential of semicircle" kernel (eq. (5)) onto a fine grid of
+ * n_i = 2 N_i points (eq. (7)), a plain FFT (eq. (9)), and truncation with
+ * correction (eq. (10)); type 2 runs the transposed steps (eq. (11), (12),
+ * Sec. II-B c).  No normalisation is applied.
+ *
+ * The interface follows the "plan, setup, execute, destroy" pattern of
+ * Sec. I-A: one plan per (type, dim, modes, iflag, eps, precision); setpts
+ * bin-sorts the points once (Sec. III-A) and any number of executes reuse
+ * them with new strengths / coefficients.
+ *
+ * Conventions for every entry point
+ *   - Return value: 0 (NUFFT_OK) on success, else a positive NUFFT_ERR_* code.
+ *     No C++ exception crosses this interface.  nufft_strerror() names codes.
+ *   - Complex arrays are interleaved (re, im) of the plan's real type:
+ *     float for dtype 0 (complex64), double for dtype 1 (complex128).
+ *   - Mode arrays f hold prod(N_i) values, k1 fastest, each k_i increasing
+ *     from -floor(N_i/2).  Point arrays c hold M values in the caller's order.
+ *   - Array pointers may be DEVICE memory (of the plan's device) or HOST
+ *     memory (pinned or pageable).  Device pointers are used in place and the
+ *     call is asynchronous on the plan's stream.  Host pointers are staged
+ *     through plan-owned device buffers and the call returns only after the
+ *     results have been copied back (synchronous).
+ *   - The caller owns every array it passes; the library keeps no pointer to
+ *     caller memory after a call returns.
+ *   - Plans are not thread safe: one plan is used by one host thread at a time.
+ */
+#ifndef NUFFT_GB300_H
+#define NUFFT_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct nufft_plan_s *nufft_plan_t;
+
+/* Error codes (returned as int). */
+#define NUFFT_OK 0
+#define NUFFT_ERR_BAD_ARG 1        /* type, dim, N, iflag, dtype, NULL pointer, M < 0 */
+#define NUFFT_ERR_BAD_EPS 2        /* eps <= 0, not finite, or width w outside [2, 16] */
+#define NUFFT_ERR_ALLOC 3          /* device (or pinned host) allocation failed */
+#define NUFFT_ERR_CUDA 4           /* a CUDA runtime call or kernel launch failed */
+#define NUFFT_ERR_CUFFT 5          /* a cuFFT call failed */
+#define NUFFT_ERR_NO_POINTS 6      /* execute before a successful setpts */
+#define NUFFT_ERR_BAD_POINTS 7     /* a coordinate is NaN or infinite */
+#define NUFFT_ERR_BAD_OPT 8        /* unknown option key or out-of-range value */
+#define NUFFT_ERR_TOO_LARGE 9      /* sizes beyond the 32-bit index ranges used inside */
+
+/* Indices of nufft_get_timings() output (milliseconds of the last execute /
+ * setpts, measured with CUDA events on the plan's stream). */
+#define NUFFT_T_SPREAD_INTERP 0    /* spreading (type 1) or interpolation (type 2) kernel */
+#define NUFFT_T_FFT 1              /* cuFFT execution */
+#define NUFFT_T_DECONV_PAD 2       /* correction + truncation (type 1) or correction + padding (type 2) */
+#define NUFFT_T_ZERO 3             /* clearing the fine grid before spreading (type 1) */
+#define NUFFT_T_EXEC 4             /* whole execute on the device (first to last event) */
+#define NUFFT_T_SETPTS 5           /* whole setpts on the device */
+#define NUFFT_T_COUNT 6
+
+/* Indices of nufft_get_info() output. */
+#define NUFFT_I_W 0                /* kernel width w (eq. (6)) */
+#define NUFFT_I_N1 1               /* fine grid n_1, n_2, n_3 (n_3 = 1 in 2D) */
+#define NUFFT_I_N2 2
+#define NUFFT_I_N3 3
+#define NUFFT_I_M 4                /* points of the last setpts */
+#define NUFFT_I_NBINS 5            /* number of bins */
+#define NUFFT_I_NSUB 6             /* number of subproblems */
+#define NUFFT_I_BIN1 7             /* bin size m_1, m_2, m_3 */
+#define NUFFT_I_BIN2 8
+#define NUFFT_I_BIN3 9
+#define NUFFT_I_MSUB 10            /* points per subproblem cap M_sub */
+#define NUFFT_I_METHOD 11          /* spreading method in use (NUFFT_METHOD_*) */
+#define NUFFT_I_COUNT 12
+
+/* Spreading / interpolation methods (option "method"). */
+#define NUFFT_METHOD_AUTO 0
+#define NUFFT_METHOD_SM 1          /* Sec. III-A "SM": subproblems spread in shared memory */
+#define NUFFT_METHOD_GM_SORT 2     /* Sec. III-A "GM-sort": thread per sorted point, global atomics */
+
+/*
+ * Create a plan.  Defined by Sec. I-A ("plan, setup, execute, destroy") and
+ * Sec. II (parameters).
+ *   type        1 or 2 (eq. (1) or eq. (3)).
+ *   dim         2 or 3.
+ *   n_modes     host array of dim entries N_1, N_2 (, N_3), each >= 1.
+ *   iflag       sign of the exponent: >= 0 -> +1, < 0 -> -1.
+ *   eps         requested relative tolerance; sets the kernel width
+ *               w = ceil(log10(1/eps)) + 1 and shape beta = 2.30 w (eq. (6)).
+ *               Accepted when 2 <= w <= 16.
+ *   dtype       0 = complex64 / float coordinates, 1 = complex128 / double.
+ *   cuda_stream cudaStream_t to enqueue all work on (NULL: the legacy default
+ *               stream).  The plan uses the device current at this call.
+ *   out         receives the plan (set to NULL on failure).
+ * Allocates the fine grid, the correction factors and the cuFFT plan on the
+ * current device.  Errors: BAD_ARG, BAD_EPS, ALLOC, CUDA, CUFFT, TOO_LARGE.
+ */
+int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double eps,
+                   int dtype, void *cuda_stream, nufft_plan_t *out);
+
+/*
+ * Set a tuning option; takes effect at the next setpts.  Keys:
+ *   "method"   NUFFT_METHOD_* (type 1 spreading; type 2 always uses the
+ *              tiled shared-memory interpolator unless "method" is GM_SORT).
+ *   "bin1", "bin2", "bin3"   bin size m_i in fine-grid cells (Sec. III-A), >= 1.
+ *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1.
+ *   "threads"  threads per block of the spreading / interpolation kernels
+ *              (multiple of 32, 32..1024).
+ * Errors: BAD_ARG (NULL), BAD_OPT (unknown key or invalid value).
+ */
+int nufft_set_opt(nufft_plan_t plan, const char *key, double value);
+
+/*
+ * Set the nonuniform points (Sec. III-A bin sort and SM step 1 subproblems).
+ *   M        number of points, >= 0 (M = 0 makes execute produce zeros / nothing).
+ *   x, y, z  M coordinates each, of the plan's real type; z is ignored (may be
+ *            NULL) in 2D.  Host or device pointers.  Read once: the plan keeps
+ *            its own sorted, grid-scaled copy, so the caller may free or
+ *            overwrite them afterwards.
+ * Synchronises the plan's stream once (to size the subproblem table).
+ * Errors: BAD_ARG, BAD_POINTS (NaN/Inf coordinate), ALLOC, CUDA, TOO_LARGE.
+ */
+int nufft_setpts(nufft_plan_t plan, int64_t M, const void *x, const void *y, const void *z);
+
+/*
+ * Run the transform on the points of the last setpts.
+ *   type 1: reads c (M complex), overwrites f (prod N_i complex).
+ *   type 2: reads f, overwrites c.
+ * Nothing is accumulated into the output.  Device pointers: asynchronous on
+ * the plan's stream.  Host pointers: synchronous (see the conventions above).
+ * Errors: BAD_ARG, NO_POINTS, ALLOC (host staging), CUDA, CUFFT.
+ */
+int nufft_execute(nufft_plan_t plan, void *c, void *f);
+
+/* Release every resource of the plan (NULL is accepted).  Synchronises the
+ * plan's stream first.  Errors: CUDA. */
+int nufft_destroy(nufft_plan_t plan);
+
+/*
+ * Device times of the last execute and setpts, in milliseconds, indexed by
+ * NUFFT_T_*.  Writes min(n, NUFFT_T_COUNT) doubles to the host array ms;
+ * entries a plan's type does not have are 0.  Waits for the recorded events.
+ * Errors: BAD_ARG, CUDA.
+ */
+int nufft_get_timings(nufft_plan_t plan, double *ms, int n);
+
+/* Plan parameters, indexed by NUFFT_I_*; writes min(n, NUFFT_I_COUNT) values
+ * to the host array info.  Errors: BAD_ARG. */
+int nufft_get_info(nufft_plan_t plan, int64_t *info, int n);
+
+/*
+ * Copy the integer results of the last setpts to HOST arrays (for checking
+ * the bin sort of Sec. III-A; any argument may be NULL to skip it):
+ *   counts[nbins]     points per bin (bins ordered x fastest);
+ *   starts[nbins]     exclusive prefix sum of counts;
+ *   perm[M]           the permutation t: sorted slot -> caller's point index
+ *                     (points of bin 0, then bin 1, ...; order inside a bin is
+ *                     unspecified);
+ *   subprob[3*nsub]   (bin, first sorted slot, point count) per subproblem.
+ * Synchronises the plan's stream.  Errors: BAD_ARG, NO_POINTS, CUDA.
+ */
+int nufft_get_sort(nufft_plan_t plan, int32_t *counts, int32_t *starts, int32_t *perm,
+                   int32_t *subprob);
+
+/* Static description of an error code. */
+const char *nufft_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NUFFT_GB300_H */

@@ -1,0 +1,120 @@
+// Internal declarations of the GB300 NUFFT library: the plan object and the
+// launchers each translation unit provides.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cufft.h>
+
+#include <cstdint>
+
+#include "../../include/nufft_gb300.h"
+
+namespace nufft {
+
+constexpr int kMaxDim = 3;
+constexpr int kMinWidth = 2;
+constexpr int kMaxWidth = 16;
+
+// One subproblem of SM step 1 (Sec. III-A of the cuFINUFFT paper): a run of
+// at most M_sub sorted points that all lie in one bin.
+struct Subproblem {
+  int32_t bin;
+  int32_t start;  // first sorted slot
+  int32_t count;  // number of points
+  int32_t pad_;
+};
+
+}  // namespace nufft
+
+struct nufft_plan_s {
+  // --- definition -------------------------------------------------------
+  int type = 1;
+  int dim = 2;
+  int iflag = -1;
+  int dtype = 0;  // 0 complex64, 1 complex128
+  double eps = 0;
+  int w = 0;
+  double beta = 0;
+  int64_t N[3] = {1, 1, 1};
+  int64_t n[3] = {1, 1, 1};
+  int device = 0;
+  cudaStream_t stream = nullptr;
+
+  // --- options (applied at setpts) --------------------------------------
+  int opt_method = NUFFT_METHOD_AUTO;
+  int opt_bin[3] = {0, 0, 0};  // 0: default
+  int opt_msub = 0;            // 0: default
+  int opt_threads = 0;         // 0: default
+
+  // --- resolved at setpts ------------------------------------------------
+  int method = NUFFT_METHOD_SM;
+  int m[3] = {1, 1, 1};
+  int nb[3] = {1, 1, 1};
+  int msub = 1024;
+  int threads = 256;
+  int64_t nbins = 0;
+  int64_t nsub = 0;
+  int64_t M = 0;
+  bool have_pts = false;
+
+  // --- device memory ----------------------------------------------------
+  void *grid = nullptr;            // fine grid, n1 n2 n3 complex, x fastest
+  void *pfac[3] = {nullptr, nullptr, nullptr};  // correction factors p_i(k), N_i reals
+  int32_t *bin_counts = nullptr;   // nbins + 1
+  int32_t *bin_starts = nullptr;   // nbins + 1 (last entry: M)
+  int32_t *sub_counts = nullptr;   // nbins + 1
+  int32_t *sub_starts = nullptr;   // nbins + 1
+  int32_t *scan_scratch = nullptr; // block partials of the scan
+  int64_t cap_bins = 0;
+  int32_t *perm = nullptr;         // M: sorted slot -> user index
+  void *gcoord[3] = {nullptr, nullptr, nullptr};  // M bin-relative grid coordinates
+  int32_t *bin_of = nullptr;       // M (setpts scratch)
+  int32_t *rank_of = nullptr;      // M (setpts scratch)
+  int64_t cap_pts = 0;
+  nufft::Subproblem *subprob = nullptr;
+  int64_t cap_sub = 0;
+  int *flag = nullptr;             // device error flag (setpts)
+  void *stage_c = nullptr;         // staging for host c
+  int64_t cap_stage_c = 0;
+  void *stage_f = nullptr;         // staging for host f
+  void *stage_xyz = nullptr;       // staging for host coordinates (3 M reals)
+  int64_t cap_stage_xyz = 0;
+
+  cufftHandle fft = 0;
+  bool fft_made = false;
+
+  // --- timing -------------------------------------------------------------
+  cudaEvent_t ev[8] = {};
+  bool ev_made = false;
+  bool exec_recorded = false;
+  bool setpts_recorded = false;
+};
+
+namespace nufft {
+
+inline size_t real_size(const nufft_plan_s *p) { return p->dtype == 0 ? 4 : 8; }
+inline int64_t grid_cells(const nufft_plan_s *p) { return p->n[0] * p->n[1] * p->n[2]; }
+inline int64_t mode_count(const nufft_plan_s *p) { return p->N[0] * p->N[1] * p->N[2]; }
+
+// setpts.cu: bin sort and subproblem table.  Returns a NUFFT_* code.
+int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z);
+
+// spreadinterp_*.cu: type 1 spreading (grid must be zeroed) and type 2
+// interpolation, for the plan's dim, dtype and width.
+// Explicitly instantiated in spreadinterp_{2,3}d_{f32,f64}.cu.
+template <int DIM, typename T>
+cudaError_t launch_spread_t(const nufft_plan_s *p, const void *c);
+template <int DIM, typename T>
+cudaError_t launch_interp_t(const nufft_plan_s *p, void *c);
+
+// deconv.cu: type 1 correction + truncation, type 2 correction + padding.
+cudaError_t launch_deconvolve(const nufft_plan_s *p, void *f);
+cudaError_t launch_pad(const nufft_plan_s *p, const void *f);
+
+// scan.cu: exclusive prefix sum of n int32 values; out has n + 1 entries and
+// out[n] receives the total.  scratch holds scan_scratch_len(n) ints.
+int64_t scan_scratch_len(int64_t n);
+cudaError_t exclusive_scan(const int32_t *in, int32_t *out, int64_t n, int32_t *scratch,
+                           cudaStream_t s);
+
+}  // namespace nufft

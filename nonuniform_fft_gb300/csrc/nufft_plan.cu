@@ -1,0 +1,538 @@
+// Plan object and C ABI of the GB300 NUFFT library (declared in
+// include/nufft_gb300.h).
+//
+// Source: "cuFINUFFT: a load-balanced GPU library for general-purpose
+// nonuniform FFTs" (Shih, Wright, Anden, Blaschke, Barnett).  The plan holds
+// the parameters of Sec. II (width and shape from eq. (6), fine grid sizes,
+// correction factors of eq. (10)), the fine grid, the cuFFT plan used for
+// eq. (9) / (12), and the bin-sort results of Sec. III-A that setpts
+// produces; execute runs the three steps on the plan's stream.
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "nufft_internal.cuh"
+
+using nufft::real_size;
+
+namespace {
+
+constexpr double kPi = 3.14159265358979323846;
+
+// ---------------------------------------------------------------- parameters
+
+// Kernel width from eq. (6): w = ceil(log10(1/eps)) + 1.  A tolerance whose
+// log10 is within 1e-9 of an integer counts as that power of ten, so that
+// decimal literals such as 1e-6 give w = 7.
+int width_for(double eps) {
+  double L = -std::log10(eps);
+  const double r = std::nearbyint(L);
+  if (std::fabs(L - r) < 1e-9) L = r;
+  return (int)std::ceil(L) + 1;
+}
+
+// Smallest 2^a 3^b 5^c >= v.
+int64_t next_smooth(int64_t v) {
+  for (int64_t n = v < 1 ? 1 : v;; n++) {
+    int64_t m = n;
+    for (int64_t f : {2, 3, 5})
+      while (m % f == 0) m /= f;
+    if (m == 1) return n;
+  }
+}
+
+// Gauss-Legendre rule on [-1, 1] by Newton iteration on P_q.
+void gauss_legendre(int q, std::vector<double> &x, std::vector<double> &wts) {
+  x.resize(q);
+  wts.resize(q);
+  for (int i = 0; i < q; i++) {
+    double t = std::cos(kPi * (4.0 * i + 3.0) / (4.0 * q + 2.0));
+    double p_q = 0, p_q1 = 0;
+    for (int it = 0; it < 100; it++) {
+      double a = 1.0, b = t;  // P_0, P_1
+      for (int k = 2; k <= q; k++) {
+        const double c = ((2 * k - 1) * t * b - (k - 1) * a) / k;
+        a = b;
+        b = c;
+      }
+      p_q = b;
+      p_q1 = a;
+      const double dp = q * (t * p_q - p_q1) / (t * t - 1.0);
+      const double step = p_q / dp;
+      t -= step;
+      if (std::fabs(step) < 1e-16) break;
+    }
+    double a = 1.0, b = t;
+    for (int k = 2; k <= q; k++) {
+      const double c = ((2 * k - 1) * t * b - (k - 1) * a) / k;
+      a = b;
+      b = c;
+    }
+    const double dp = q * (t * b - a) / (t * t - 1.0);
+    x[i] = t;
+    wts[i] = 2.0 / ((1.0 - t * t) * dp * dp);
+  }
+}
+
+// Correction factors p(k) = (2/w) / phihat(alpha k), alpha = w pi / n, for the
+// modes k of I_N in increasing order (text after eq. (10)).  phihat is the
+// Fourier transform (eq. (4)) of the ES kernel (eq. (5)),
+//   phihat(xi) = 2 int_0^1 exp(beta (sqrt(1 - z^2) - 1)) cos(xi z) dz,
+// taken with z = sin(theta) so that the integrand is smooth:
+//   2 int_0^{pi/2} exp(beta (cos theta - 1)) cos(xi sin theta) cos theta dtheta.
+std::vector<double> correction_factors(int64_t N, int64_t n, int w, double beta) {
+  std::vector<double> gx, gw;
+  gauss_legendre(100, gx, gw);
+  std::vector<double> th(gx.size()), wt(gx.size());
+  for (size_t i = 0; i < gx.size(); i++) {
+    th[i] = (gx[i] + 1.0) * (kPi / 4.0);
+    wt[i] = gw[i] * (kPi / 4.0) * std::exp(beta * (std::cos(th[i]) - 1.0)) * std::cos(th[i]);
+  }
+  const double alpha = w * kPi / (double)n;
+  std::vector<double> p((size_t)N);
+  const int64_t kmin = -(N / 2);
+  for (int64_t i = 0; i < N; i++) {
+    const double xi = alpha * (double)(kmin + i);
+    double s = 0.0;
+    for (size_t q = 0; q < th.size(); q++) s += wt[q] * std::cos(xi * std::sin(th[q]));
+    p[(size_t)i] = (2.0 / w) / (2.0 * s);
+  }
+  return p;
+}
+
+// ---------------------------------------------------------------- helpers
+
+bool is_device_ptr(const void *ptr, int device, bool *ok) {
+  cudaPointerAttributes attr;
+  *ok = true;
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state
+    return false;       // unknown to CUDA: pageable host memory
+  }
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) {
+    if (attr.type == cudaMemoryTypeDevice && attr.device != device) *ok = false;
+    return true;
+  }
+  return false;  // pinned or unregistered host memory
+}
+
+int grow_buffer(void **buf, int64_t *cap, int64_t bytes) {
+  if (*buf && *cap >= bytes) return NUFFT_OK;
+  if (*buf) cudaFree(*buf);
+  *buf = nullptr;
+  *cap = 0;
+  if (cudaMalloc(buf, (size_t)(bytes > 0 ? bytes : 16)) != cudaSuccess) {
+    cudaGetLastError();
+    return NUFFT_ERR_ALLOC;
+  }
+  *cap = bytes;
+  return NUFFT_OK;
+}
+
+// Default bin sizes (Sec. III-A Remark 1 gives 32 x 32 in 2D): in 3D the
+// largest bins, halving the longest side, whose padded tile fits the budget.
+void default_bins(const nufft_plan_s *p, int m[3]) {
+  const int pad = (p->w + 1) / 2;
+  const size_t cs = 2 * real_size(p);
+  if (p->dim == 2) {
+    m[0] = m[1] = 32;
+    m[2] = 1;
+  } else {
+    m[0] = m[1] = 16;
+    m[2] = 8;
+    const size_t budget = p->dtype == 0 ? 96 * 1024 : 200 * 1024;
+    for (;;) {
+      const size_t bytes = (size_t)(m[0] + 2 * pad) * (m[1] + 2 * pad) * (m[2] + 2 * pad) * cs;
+      if (bytes <= budget || (m[0] == 1 && m[1] == 1 && m[2] == 1)) break;
+      int d = 0;
+      for (int i = 1; i < 3; i++)
+        if (m[i] > m[d]) d = i;
+      m[d] = (m[d] + 1) / 2;
+    }
+  }
+}
+
+size_t tile_bytes(const nufft_plan_s *p, const int m[3]) {
+  const int pad = (p->w + 1) / 2;
+  size_t cells = 1;
+  for (int d = 0; d < p->dim; d++) cells *= (size_t)(m[d] + 2 * pad);
+  return cells * 2 * real_size(p);
+}
+
+void release(nufft_plan_s *p) {
+  cudaFree(p->grid);
+  for (int d = 0; d < 3; d++) {
+    cudaFree(p->pfac[d]);
+    cudaFree(p->gcoord[d]);
+  }
+  cudaFree(p->bin_counts);
+  cudaFree(p->bin_starts);
+  cudaFree(p->sub_counts);
+  cudaFree(p->sub_starts);
+  cudaFree(p->scan_scratch);
+  cudaFree(p->perm);
+  cudaFree(p->bin_of);
+  cudaFree(p->rank_of);
+  cudaFree(p->subprob);
+  cudaFree(p->flag);
+  cudaFree(p->stage_c);
+  cudaFree(p->stage_f);
+  cudaFree(p->stage_xyz);
+  if (p->fft_made) cufftDestroy(p->fft);
+  if (p->ev_made)
+    for (auto &e : p->ev) cudaEventDestroy(e);
+}
+
+int cuda_code(cudaError_t e) {
+  if (e == cudaSuccess) return NUFFT_OK;
+  if (e == cudaErrorMemoryAllocation) return NUFFT_ERR_ALLOC;
+  return NUFFT_ERR_CUDA;
+}
+
+// Event slots.
+enum { EV_A = 0, EV_B, EV_C, EV_D, EV_E, EV_SET0 = 6, EV_SET1 = 7 };
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+const char *nufft_strerror(int code) {
+  switch (code) {
+    case NUFFT_OK: return "success";
+    case NUFFT_ERR_BAD_ARG: return "invalid argument";
+    case NUFFT_ERR_BAD_EPS: return "tolerance out of range (kernel width must be 2..16)";
+    case NUFFT_ERR_ALLOC: return "memory allocation failed";
+    case NUFFT_ERR_CUDA: return "CUDA runtime error";
+    case NUFFT_ERR_CUFFT: return "cuFFT error";
+    case NUFFT_ERR_NO_POINTS: return "execute called before a successful setpts";
+    case NUFFT_ERR_BAD_POINTS: return "a point coordinate is NaN or infinite";
+    case NUFFT_ERR_BAD_OPT: return "unknown option or invalid option value";
+    case NUFFT_ERR_TOO_LARGE: return "problem size beyond the supported index range";
+    default: return "unknown error code";
+  }
+}
+
+int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double eps, int dtype,
+                   void *cuda_stream, nufft_plan_t *out) {
+  if (out) *out = nullptr;
+  if (!out || !n_modes || (type != 1 && type != 2) || (dim != 2 && dim != 3) ||
+      (dtype != 0 && dtype != 1))
+    return NUFFT_ERR_BAD_ARG;
+  for (int d = 0; d < dim; d++)
+    if (n_modes[d] < 1) return NUFFT_ERR_BAD_ARG;
+  if (!(eps > 0) || !std::isfinite(eps)) return NUFFT_ERR_BAD_EPS;
+  const int w = width_for(eps);
+  if (w < nufft::kMinWidth || w > nufft::kMaxWidth) return NUFFT_ERR_BAD_EPS;
+
+  nufft_plan_s *p = new (std::nothrow) nufft_plan_s();
+  if (!p) return NUFFT_ERR_ALLOC;
+  p->type = type;
+  p->dim = dim;
+  p->iflag = iflag >= 0 ? 1 : -1;
+  p->dtype = dtype;
+  p->eps = eps;
+  p->w = w;
+  p->beta = 2.30 * w;
+  int64_t cells = 1, modes = 1;
+  for (int d = 0; d < dim; d++) {
+    p->N[d] = n_modes[d];
+    if (p->N[d] > (int64_t(1) << 29)) {
+      delete p;
+      return NUFFT_ERR_TOO_LARGE;
+    }
+    p->n[d] = next_smooth(std::max<int64_t>(2 * p->N[d], 2 * (int64_t)w));
+    cells *= p->n[d];
+    modes *= p->N[d];
+  }
+  if (cells > (int64_t(1) << 36) || modes > (int64_t(1) << 34)) {
+    delete p;
+    return NUFFT_ERR_TOO_LARGE;
+  }
+  p->stream = static_cast<cudaStream_t>(cuda_stream);
+  int rc = NUFFT_OK;
+  do {
+    if (cudaGetDevice(&p->device) != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
+    const size_t rs = real_size(p);
+    if (cudaMalloc(&p->grid, (size_t)cells * 2 * rs) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
+    for (int d = 0; d < dim; d++) {
+      std::vector<double> pf = correction_factors(p->N[d], p->n[d], w, p->beta);
+      if (cudaMalloc(&p->pfac[d], pf.size() * rs) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
+      cudaError_t e;
+      if (dtype == 0) {
+        std::vector<float> pf32(pf.begin(), pf.end());
+        e = cudaMemcpy(p->pfac[d], pf32.data(), pf32.size() * 4, cudaMemcpyHostToDevice);
+      } else {
+        e = cudaMemcpy(p->pfac[d], pf.data(), pf.size() * 8, cudaMemcpyHostToDevice);
+      }
+      if (e != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
+    }
+    if (rc) break;
+    // cuFFT: row-major dims, slowest first (our x index is fastest)
+    cufftResult fr;
+    const cufftType ft = dtype == 0 ? CUFFT_C2C : CUFFT_Z2Z;
+    if (dim == 2)
+      fr = cufftPlan2d(&p->fft, (int)p->n[1], (int)p->n[0], ft);
+    else
+      fr = cufftPlan3d(&p->fft, (int)p->n[2], (int)p->n[1], (int)p->n[0], ft);
+    if (fr != CUFFT_SUCCESS) { rc = fr == CUFFT_ALLOC_FAILED ? NUFFT_ERR_ALLOC : NUFFT_ERR_CUFFT; break; }
+    p->fft_made = true;
+    if (cufftSetStream(p->fft, p->stream) != CUFFT_SUCCESS) { rc = NUFFT_ERR_CUFFT; break; }
+    for (auto &e : p->ev)
+      if (cudaEventCreate(&e) != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
+    if (rc) break;
+    p->ev_made = true;
+  } while (false);
+  if (rc) {
+    cudaGetLastError();
+    release(p);
+    delete p;
+    return rc;
+  }
+  *out = p;
+  return NUFFT_OK;
+}
+
+int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
+  if (!p || !key) return NUFFT_ERR_BAD_ARG;
+  if (!std::isfinite(value) || value != std::floor(value)) return NUFFT_ERR_BAD_OPT;
+  const int64_t v = (int64_t)value;
+  if (!std::strcmp(key, "method")) {
+    if (v != NUFFT_METHOD_AUTO && v != NUFFT_METHOD_SM && v != NUFFT_METHOD_GM_SORT) return NUFFT_ERR_BAD_OPT;
+    p->opt_method = (int)v;
+  } else if (!std::strcmp(key, "bin1") || !std::strcmp(key, "bin2") || !std::strcmp(key, "bin3")) {
+    if (v < 0 || v > 4096) return NUFFT_ERR_BAD_OPT;
+    p->opt_bin[key[3] - '1'] = (int)v;
+  } else if (!std::strcmp(key, "msub")) {
+    if (v < 0 || v > (int64_t(1) << 24)) return NUFFT_ERR_BAD_OPT;
+    p->opt_msub = (int)v;
+  } else if (!std::strcmp(key, "threads")) {
+    if (v != 0 && (v < 32 || v > 1024 || v % 32)) return NUFFT_ERR_BAD_OPT;
+    p->opt_threads = (int)v;
+  } else {
+    return NUFFT_ERR_BAD_OPT;
+  }
+  return NUFFT_OK;
+}
+
+int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const void *z) {
+  if (!p || M < 0 || (M > 0 && (!x || !y || (p->dim == 3 && !z)))) return NUFFT_ERR_BAD_ARG;
+  if (M > (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
+  p->have_pts = false;
+  if (cudaSetDevice(p->device) != cudaSuccess) return NUFFT_ERR_CUDA;
+
+  // resolve options
+  p->method = p->opt_method == NUFFT_METHOD_AUTO ? NUFFT_METHOD_SM : p->opt_method;
+  int m[3];
+  default_bins(p, m);
+  for (int d = 0; d < 3; d++) {
+    if (d < p->dim && p->opt_bin[d] > 0) m[d] = p->opt_bin[d];
+    if (d >= p->dim) m[d] = 1;
+    if (m[d] > p->n[d]) m[d] = (int)p->n[d];
+  }
+  int smem_max = 0;
+  if (cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, p->device) != cudaSuccess)
+    return NUFFT_ERR_CUDA;
+  if (p->method == NUFFT_METHOD_SM && tile_bytes(p, m) > (size_t)smem_max) return NUFFT_ERR_BAD_OPT;
+  p->nbins = 1;
+  for (int d = 0; d < 3; d++) {
+    p->m[d] = m[d];
+    p->nb[d] = (int)((p->n[d] + m[d] - 1) / m[d]);
+    p->nbins *= p->nb[d];
+  }
+  p->msub = p->opt_msub > 0 ? p->opt_msub : 1024;
+  p->threads = p->opt_threads > 0 ? p->opt_threads : 256;
+  p->M = M;
+
+  // coordinates in host memory are staged through a device buffer
+  const void *xyz[3] = {x, y, p->dim == 3 ? z : nullptr};
+  if (M > 0) {
+    const size_t bytes = (size_t)M * real_size(p);
+    for (int d = 0; d < p->dim; d++) {
+      bool ok;
+      if (is_device_ptr(xyz[d], p->device, &ok)) {
+        if (!ok) return NUFFT_ERR_BAD_ARG;
+        continue;
+      }
+      int rc = grow_buffer(&p->stage_xyz, &p->cap_stage_xyz, (int64_t)(3 * bytes));
+      if (rc) return rc;
+      void *dst = static_cast<char *>(p->stage_xyz) + d * bytes;
+      if (cudaMemcpyAsync(dst, xyz[d], bytes, cudaMemcpyHostToDevice, p->stream) != cudaSuccess)
+        return NUFFT_ERR_CUDA;
+      xyz[d] = dst;
+    }
+  }
+  if (cudaEventRecord(p->ev[EV_SET0], p->stream) != cudaSuccess) return NUFFT_ERR_CUDA;
+  const int rc = nufft::run_setpts(p, xyz[0], xyz[1], xyz[2]);
+  if (rc) {
+    cudaGetLastError();
+    return rc;
+  }
+  if (cudaEventRecord(p->ev[EV_SET1], p->stream) != cudaSuccess) return NUFFT_ERR_CUDA;
+  p->setpts_recorded = true;
+  p->have_pts = true;
+  return NUFFT_OK;
+}
+
+int nufft_execute(nufft_plan_t p, void *c, void *f) {
+  if (!p) return NUFFT_ERR_BAD_ARG;
+  if (!p->have_pts) return NUFFT_ERR_NO_POINTS;
+  if (!f || (p->M > 0 && !c)) return NUFFT_ERR_BAD_ARG;
+  if (cudaSetDevice(p->device) != cudaSuccess) return NUFFT_ERR_CUDA;
+  cudaStream_t s = p->stream;
+  const size_t cb = 2 * real_size(p);
+  const size_t c_bytes = (size_t)p->M * cb, f_bytes = (size_t)nufft::mode_count(p) * cb;
+
+  // stage host arrays
+  bool ok = true;
+  const bool c_host = p->M > 0 && !is_device_ptr(c, p->device, &ok);
+  if (!ok) return NUFFT_ERR_BAD_ARG;
+  const bool f_host = !is_device_ptr(f, p->device, &ok);
+  if (!ok) return NUFFT_ERR_BAD_ARG;
+  void *dc = c, *df = f;
+  int rc;
+  if (c_host) {
+    if ((rc = grow_buffer(&p->stage_c, &p->cap_stage_c, (int64_t)c_bytes))) return rc;
+    dc = p->stage_c;
+    if (p->type == 1 && cudaMemcpyAsync(dc, c, c_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
+  }
+  if (f_host) {
+    if (!p->stage_f && cudaMalloc(&p->stage_f, f_bytes) != cudaSuccess) return NUFFT_ERR_ALLOC;
+    df = p->stage_f;
+    if (p->type == 2 && cudaMemcpyAsync(df, f, f_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
+  }
+
+  const int dir = p->iflag >= 0 ? CUFFT_INVERSE : CUFFT_FORWARD;
+  auto fft = [&]() -> int {
+    cufftResult r = p->dtype == 0
+                        ? cufftExecC2C(p->fft, (cufftComplex *)p->grid, (cufftComplex *)p->grid, dir)
+                        : cufftExecZ2Z(p->fft, (cufftDoubleComplex *)p->grid,
+                                       (cufftDoubleComplex *)p->grid, dir);
+    return r == CUFFT_SUCCESS ? NUFFT_OK : NUFFT_ERR_CUFFT;
+  };
+  auto spread = [&]() -> cudaError_t {
+    if (p->nsub == 0) return cudaSuccess;
+    if (p->dim == 2)
+      return p->dtype == 0 ? nufft::launch_spread_t<2, float>(p, dc) : nufft::launch_spread_t<2, double>(p, dc);
+    return p->dtype == 0 ? nufft::launch_spread_t<3, float>(p, dc) : nufft::launch_spread_t<3, double>(p, dc);
+  };
+  auto interp = [&]() -> cudaError_t {
+    if (p->nsub == 0) return cudaSuccess;
+    if (p->dim == 2)
+      return p->dtype == 0 ? nufft::launch_interp_t<2, float>(p, dc) : nufft::launch_interp_t<2, double>(p, dc);
+    return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);
+  };
+
+  cudaError_t e;
+  if (p->type == 1) {
+    // zero -> spread (eq. (7)) -> FFT (eq. (9)) -> correct + truncate (eq. (10))
+    if ((e = cudaEventRecord(p->ev[EV_A], s)) != cudaSuccess) return cuda_code(e);
+    if ((e = cudaMemsetAsync(p->grid, 0, (size_t)nufft::grid_cells(p) * cb, s)) != cudaSuccess) return cuda_code(e);
+    if ((e = cudaEventRecord(p->ev[EV_B], s)) != cudaSuccess) return cuda_code(e);
+    if ((e = spread()) != cudaSuccess) return cuda_code(e);
+    if ((e = cudaEventRecord(p->ev[EV_C], s)) != cudaSuccess) return cuda_code(e);
+    if ((rc = fft())) return rc;
+    if ((e = cudaEventRecord(p->ev[EV_D], s)) != cudaSuccess) return cuda_code(e);
+    if ((e = nufft::launch_deconvolve(p, df)) != cudaSuccess) return cuda_code(e);
+    if ((e = cudaEventRecord(p->ev[EV_E], s)) != cudaSuccess) return cuda_code(e);
+  } else {
+    // correct + pad (eq. (11)) -> FFT (eq. (12)) -> interpolate (Sec. II-B c)
+    if ((e = cudaEventRecord(p->ev[EV_A], s)) != cudaSuccess) return cuda_code(e);
+    if (p->M > 0) {
+      if ((e = nufft::launch_pad(p, df)) != cudaSuccess) return cuda_code(e);
+    }
+    if ((e = cudaEventRecord(p->ev[EV_B], s)) != cudaSuccess) return cuda_code(e);
+    if (p->M > 0 && (rc = fft())) return rc;
+    if ((e = cudaEventRecord(p->ev[EV_C], s)) != cudaSuccess) return cuda_code(e);
+    if ((e = interp()) != cudaSuccess) return cuda_code(e);
+    if ((e = cudaEventRecord(p->ev[EV_D], s)) != cudaSuccess) return cuda_code(e);
+  }
+  p->exec_recorded = true;
+
+  // copy host results back and wait for them
+  if (p->type == 1 && f_host) {
+    if (cudaMemcpyAsync(f, df, f_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+  if (p->type == 2 && c_host) {
+    if (cudaMemcpyAsync(c, dc, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+  if (c_host || f_host) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+  return NUFFT_OK;
+}
+
+int nufft_destroy(nufft_plan_t p) {
+  if (!p) return NUFFT_OK;
+  cudaSetDevice(p->device);
+  const cudaError_t e = cudaStreamSynchronize(p->stream);
+  release(p);
+  delete p;
+  return e == cudaSuccess ? NUFFT_OK : NUFFT_ERR_CUDA;
+}
+
+int nufft_get_timings(nufft_plan_t p, double *ms, int n) {
+  if (!p || !ms || n < 0) return NUFFT_ERR_BAD_ARG;
+  double t[NUFFT_T_COUNT] = {0, 0, 0, 0, 0, 0};
+  auto span = [&](int a, int b, double *dst) -> int {
+    float v = 0;
+    if (cudaEventSynchronize(p->ev[b]) != cudaSuccess) return NUFFT_ERR_CUDA;
+    if (cudaEventElapsedTime(&v, p->ev[a], p->ev[b]) != cudaSuccess) return NUFFT_ERR_CUDA;
+    *dst = v;
+    return NUFFT_OK;
+  };
+  int rc;
+  if (p->exec_recorded) {
+    if (p->type == 1) {
+      if ((rc = span(EV_A, EV_B, &t[NUFFT_T_ZERO])) || (rc = span(EV_B, EV_C, &t[NUFFT_T_SPREAD_INTERP])) ||
+          (rc = span(EV_C, EV_D, &t[NUFFT_T_FFT])) || (rc = span(EV_D, EV_E, &t[NUFFT_T_DECONV_PAD])) ||
+          (rc = span(EV_A, EV_E, &t[NUFFT_T_EXEC])))
+        return rc;
+    } else {
+      if ((rc = span(EV_A, EV_B, &t[NUFFT_T_DECONV_PAD])) || (rc = span(EV_B, EV_C, &t[NUFFT_T_FFT])) ||
+          (rc = span(EV_C, EV_D, &t[NUFFT_T_SPREAD_INTERP])) || (rc = span(EV_A, EV_D, &t[NUFFT_T_EXEC])))
+        return rc;
+    }
+  }
+  if (p->setpts_recorded && (rc = span(EV_SET0, EV_SET1, &t[NUFFT_T_SETPTS]))) return rc;
+  for (int i = 0; i < n && i < NUFFT_T_COUNT; i++) ms[i] = t[i];
+  return NUFFT_OK;
+}
+
+int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
+  if (!p || !info || n < 0) return NUFFT_ERR_BAD_ARG;
+  const int64_t v[NUFFT_I_COUNT] = {p->w,     p->n[0],  p->n[1],  p->n[2], p->M,    p->nbins,
+                                    p->nsub,  p->m[0],  p->m[1],  p->m[2], p->msub, p->method};
+  for (int i = 0; i < n && i < NUFFT_I_COUNT; i++) info[i] = v[i];
+  return NUFFT_OK;
+}
+
+int nufft_get_sort(nufft_plan_t p, int32_t *counts, int32_t *starts, int32_t *perm, int32_t *subprob) {
+  if (!p) return NUFFT_ERR_BAD_ARG;
+  if (!p->have_pts) return NUFFT_ERR_NO_POINTS;
+  if (cudaSetDevice(p->device) != cudaSuccess || cudaStreamSynchronize(p->stream) != cudaSuccess)
+    return NUFFT_ERR_CUDA;
+  const size_t nb = (size_t)p->nbins * 4;
+  if (counts && cudaMemcpy(counts, p->bin_counts, nb, cudaMemcpyDeviceToHost) != cudaSuccess) return NUFFT_ERR_CUDA;
+  if (starts && cudaMemcpy(starts, p->bin_starts, nb, cudaMemcpyDeviceToHost) != cudaSuccess) return NUFFT_ERR_CUDA;
+  if (perm && p->M > 0 && cudaMemcpy(perm, p->perm, (size_t)p->M * 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return NUFFT_ERR_CUDA;
+  if (subprob && p->nsub > 0) {
+    std::vector<nufft::Subproblem> tmp((size_t)p->nsub);
+    if (cudaMemcpy(tmp.data(), p->subprob, tmp.size() * sizeof(nufft::Subproblem), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+      return NUFFT_ERR_CUDA;
+    for (size_t i = 0; i < tmp.size(); i++) {
+      subprob[3 * i] = tmp[i].bin;
+      subprob[3 * i + 1] = tmp[i].start;
+      subprob[3 * i + 2] = tmp[i].count;
+    }
+  }
+  return NUFFT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,422 @@
+// Spreading (type 1 step 1) and interpolation (type 2 step 3) kernels.
+//
+// Source: "cuFINUFFT: a load-balanced GPU library for general-purpose
+// nonuniform FFTs" (Shih, Wright, Anden, Blaschke, Barnett):
+//   - spreading b_l = sum_j c_j psi_per(l h - x_j), eq. (7)-(8), with the ES
+//     kernel phi_beta(z) = exp(beta (sqrt(1 - z^2) - 1)), eq. (5);
+//   - "SM" (Sec. III-A, Fig. 1): one thread block per subproblem (at most
+//     M_sub points of one bin), spreading into a shared-memory copy of the
+//     padded bin, p_i = m_i + 2 ceil(w/2) (eq. (13)-(14)), then adding the
+//     padded bin back into the fine grid with periodic wrapping (eq. (15));
+//   - "GM-sort" (Sec. III-A / III-B): the same sorted traversal without the
+//     shared-memory copy, reading / atomically adding the fine grid directly;
+//   - interpolation c_j = sum_l b_l psi_per(l h - x_j) (Sec. II-B c) over the
+//     sorted points; the SM variant first stages the padded bin of the fine
+//     grid in shared memory and then reads only shared memory.
+//
+// Point data come from setpts: for sorted slot j, perm[j] is the caller's
+// index and g_d[j] the coordinate in fine-grid cells relative to the origin
+// of the point's bin, in [0, m_d].  Node l (bin-relative) has kernel argument
+// z = (l - g) 2 / w; the w nodes taken are l0 .. l0 + w - 1, l0 = ceil(g - w/2),
+// i.e. every node with z in [-1, 1).
+#pragma once
+
+#include "nufft_internal.cuh"
+
+namespace nufft {
+
+template <typename T> struct Cplx;
+template <> struct Cplx<float> { using type = float2; };
+template <> struct Cplx<double> { using type = double2; };
+
+__device__ __forceinline__ float es_exp(float v) { return expf(v); }
+__device__ __forceinline__ double es_exp(double v) { return exp(v); }
+__device__ __forceinline__ float es_sqrt(float v) { return sqrtf(v); }
+__device__ __forceinline__ double es_sqrt(double v) { return sqrt(v); }
+__device__ __forceinline__ float es_ceil(float v) { return ceilf(v); }
+__device__ __forceinline__ double es_ceil(double v) { return ceil(v); }
+
+// Kernel values of one point in one dimension: k[t] = phi_beta(z_t) for the
+// w nodes l0 + t.  Returns l0 (relative to the bin origin).
+template <typename T, int W>
+__device__ __forceinline__ int es_weights(T g, T beta, T (&k)[W]) {
+  const T l0 = es_ceil(g - T(0.5) * T(W));
+  const T d = l0 - g;
+  const T scale = T(2) / T(W);
+#pragma unroll
+  for (int t = 0; t < W; t++) {
+    const T z = (d + T(t)) * scale;
+    T q = (T(1) - z) * (T(1) + z);
+    q = q > T(0) ? q : T(0);
+    k[t] = es_exp(beta * (es_sqrt(q) - T(1)));
+  }
+  return (int)l0;
+}
+
+__device__ __forceinline__ void grid_atomic_add(float2 *cell, float re, float im) {
+  atomicAdd(cell, make_float2(re, im));
+}
+__device__ __forceinline__ void grid_atomic_add(double2 *cell, double re, double im) {
+  atomicAdd(&cell->x, re);
+  atomicAdd(&cell->y, im);
+}
+
+// Periodic wrap of a node index that is at most one period out of [0, n)
+// (a point's own support: l in [-w, n + w), n >= 2w).
+__device__ __forceinline__ int wrap_once(int l, int n) {
+  return l < 0 ? l + n : (l >= n ? l - n : l);
+}
+
+// Periodic wrap of a padded-tile node, o + s in [-pad, 3n): the last bin of a
+// dimension can be narrower than m, so its padded tile may reach past 2n.
+__device__ __forceinline__ int wrap_tile(int l, int n) {
+  if (l < 0) return l + n;
+  while (l >= n) l -= n;
+  return l;
+}
+
+template <typename T>
+struct SIParams {
+  using C = typename Cplx<T>::type;
+  const Subproblem *sub;
+  const int32_t *perm;
+  const T *g1, *g2, *g3;
+  C *grid;
+  const C *c_in;  // type 1 strengths (caller's order)
+  C *c_out;       // type 2 results (caller's order)
+  T beta;
+  int n1, n2, n3;
+  int m1, m2, m3;
+  int nb1, nb2;
+};
+
+// Bin coordinates of a bin index (x fastest).
+template <int DIM>
+__device__ __forceinline__ void bin_coords(int bin, int nb1, int nb2, int &b1, int &b2, int &b3) {
+  b1 = bin % nb1;
+  const int r = bin / nb1;
+  if (DIM == 3) {
+    b2 = r % nb2;
+    b3 = r / nb2;
+  } else {
+    b2 = r;
+    b3 = 0;
+  }
+}
+
+// ---------------------------------------------------------------- SM spread
+template <typename T, int DIM, int W>
+__global__ void spread_sm_kernel(SIParams<T> a) {
+  using C = typename Cplx<T>::type;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T *tile = reinterpret_cast<T *>(smem_raw);  // interleaved (re, im)
+  constexpr int PAD = (W + 1) / 2;
+  const Subproblem sp = a.sub[blockIdx.x];
+  int b1, b2, b3;
+  bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
+  const int p1 = a.m1 + 2 * PAD, p2 = a.m2 + 2 * PAD, p3 = DIM == 3 ? a.m3 + 2 * PAD : 1;
+  const int ncell = p1 * p2 * p3;
+  for (int i = threadIdx.x; i < 2 * ncell; i += blockDim.x) tile[i] = T(0);
+  __syncthreads();
+
+  const int end = sp.start + sp.count;
+  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+    const C cv = a.c_in[a.perm[j]];
+    T k1[W], k2[W], k3[W];
+    const int s1 = es_weights<T, W>(a.g1[j], a.beta, k1) + PAD;
+    const int s2 = es_weights<T, W>(a.g2[j], a.beta, k2) + PAD;
+    int s3 = 0;
+    if (DIM == 3) s3 = es_weights<T, W>(a.g3[j], a.beta, k3) + PAD;
+#pragma unroll 1
+    for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+      const T v3 = DIM == 3 ? k3[i3] : T(1);
+#pragma unroll
+      for (int i2 = 0; i2 < W; i2++) {
+        const T v = k2[i2] * v3;
+        const T vr = cv.x * v, vi = cv.y * v;
+        T *row = tile + 2 * (((s3 + i3) * p2 + s2 + i2) * p1 + s1);
+#pragma unroll
+        for (int i1 = 0; i1 < W; i1++) {
+          atomicAdd(row + 2 * i1, vr * k1[i1]);
+          atomicAdd(row + 2 * i1 + 1, vi * k1[i1]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // add the padded bin back into the fine grid, wrapping periodically (eq. (15))
+  const int o1 = b1 * a.m1 - PAD, o2 = b2 * a.m2 - PAD, o3 = DIM == 3 ? b3 * a.m3 - PAD : 0;
+  for (int i = threadIdx.x; i < ncell; i += blockDim.x) {
+    const T re = tile[2 * i], im = tile[2 * i + 1];
+    if (re == T(0) && im == T(0)) continue;
+    const int s1 = i % p1;
+    const int q = i / p1;
+    const int s2 = q % p2;
+    const int s3 = q / p2;
+    const int l1 = wrap_tile(o1 + s1, a.n1);
+    const int l2 = wrap_tile(o2 + s2, a.n2);
+    const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
+    grid_atomic_add(a.grid + (l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)), re, im);
+  }
+}
+
+// ---------------------------------------------------------------- GM-sort spread
+template <typename T, int DIM, int W>
+__global__ void spread_gm_kernel(SIParams<T> a) {
+  using C = typename Cplx<T>::type;
+  const Subproblem sp = a.sub[blockIdx.x];
+  int b1, b2, b3;
+  bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
+  const int end = sp.start + sp.count;
+  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+    const C cv = a.c_in[a.perm[j]];
+    T k1[W], k2[W], k3[W];
+    const int l1 = es_weights<T, W>(a.g1[j], a.beta, k1) + b1 * a.m1;
+    const int l2 = es_weights<T, W>(a.g2[j], a.beta, k2) + b2 * a.m2;
+    int l3 = 0;
+    if (DIM == 3) l3 = es_weights<T, W>(a.g3[j], a.beta, k3) + b3 * a.m3;
+    int x1[W];
+#pragma unroll
+    for (int i1 = 0; i1 < W; i1++) x1[i1] = wrap_once(l1 + i1, a.n1);
+#pragma unroll 1
+    for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+      const T v3 = DIM == 3 ? k3[i3] : T(1);
+      const int64_t z3 = DIM == 3 ? (int64_t)wrap_once(l3 + i3, a.n3) * a.n2 : 0;
+#pragma unroll
+      for (int i2 = 0; i2 < W; i2++) {
+        const T v = k2[i2] * v3;
+        const T vr = cv.x * v, vi = cv.y * v;
+        C *row = a.grid + (z3 + wrap_once(l2 + i2, a.n2)) * (int64_t)a.n1;
+#pragma unroll
+        for (int i1 = 0; i1 < W; i1++) grid_atomic_add(row + x1[i1], vr * k1[i1], vi * k1[i1]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- SM interp
+template <typename T, int DIM, int W>
+__global__ void interp_sm_kernel(SIParams<T> a) {
+  using C = typename Cplx<T>::type;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  C *tile = reinterpret_cast<C *>(smem_raw);
+  constexpr int PAD = (W + 1) / 2;
+  const Subproblem sp = a.sub[blockIdx.x];
+  int b1, b2, b3;
+  bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
+  const int p1 = a.m1 + 2 * PAD, p2 = a.m2 + 2 * PAD, p3 = DIM == 3 ? a.m3 + 2 * PAD : 1;
+  const int ncell = p1 * p2 * p3;
+  const int o1 = b1 * a.m1 - PAD, o2 = b2 * a.m2 - PAD, o3 = DIM == 3 ? b3 * a.m3 - PAD : 0;
+  // stage the padded bin of the fine grid (periodic wrap) in shared memory
+  for (int i = threadIdx.x; i < ncell; i += blockDim.x) {
+    const int s1 = i % p1;
+    const int q = i / p1;
+    const int s2 = q % p2;
+    const int s3 = q / p2;
+    const int l1 = wrap_tile(o1 + s1, a.n1);
+    const int l2 = wrap_tile(o2 + s2, a.n2);
+    const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
+    tile[i] = a.grid[l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)];
+  }
+  __syncthreads();
+
+  const int end = sp.start + sp.count;
+  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+    T k1[W], k2[W], k3[W];
+    const int s1 = es_weights<T, W>(a.g1[j], a.beta, k1) + PAD;
+    const int s2 = es_weights<T, W>(a.g2[j], a.beta, k2) + PAD;
+    int s3 = 0;
+    if (DIM == 3) s3 = es_weights<T, W>(a.g3[j], a.beta, k3) + PAD;
+    T ar = T(0), ai = T(0);
+#pragma unroll 1
+    for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+      T sr3 = T(0), si3 = T(0);
+#pragma unroll
+      for (int i2 = 0; i2 < W; i2++) {
+        const C *row = tile + ((s3 + i3) * p2 + s2 + i2) * p1 + s1;
+        T sr = T(0), si = T(0);
+#pragma unroll
+        for (int i1 = 0; i1 < W; i1++) {
+          const C b = row[i1];
+          sr += b.x * k1[i1];
+          si += b.y * k1[i1];
+        }
+        sr3 += sr * k2[i2];
+        si3 += si * k2[i2];
+      }
+      const T v3 = DIM == 3 ? k3[i3] : T(1);
+      ar += sr3 * v3;
+      ai += si3 * v3;
+    }
+    C out;
+    out.x = ar;
+    out.y = ai;
+    a.c_out[a.perm[j]] = out;
+  }
+}
+
+// ---------------------------------------------------------------- GM-sort interp
+template <typename T, int DIM, int W>
+__global__ void interp_gm_kernel(SIParams<T> a) {
+  using C = typename Cplx<T>::type;
+  const Subproblem sp = a.sub[blockIdx.x];
+  int b1, b2, b3;
+  bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
+  const int end = sp.start + sp.count;
+  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+    T k1[W], k2[W], k3[W];
+    const int l1 = es_weights<T, W>(a.g1[j], a.beta, k1) + b1 * a.m1;
+    const int l2 = es_weights<T, W>(a.g2[j], a.beta, k2) + b2 * a.m2;
+    int l3 = 0;
+    if (DIM == 3) l3 = es_weights<T, W>(a.g3[j], a.beta, k3) + b3 * a.m3;
+    int x1[W];
+#pragma unroll
+    for (int i1 = 0; i1 < W; i1++) x1[i1] = wrap_once(l1 + i1, a.n1);
+    T ar = T(0), ai = T(0);
+#pragma unroll 1
+    for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+      const int64_t z3 = DIM == 3 ? (int64_t)wrap_once(l3 + i3, a.n3) * a.n2 : 0;
+      T sr3 = T(0), si3 = T(0);
+#pragma unroll
+      for (int i2 = 0; i2 < W; i2++) {
+        const C *row = a.grid + (z3 + wrap_once(l2 + i2, a.n2)) * (int64_t)a.n1;
+        T sr = T(0), si = T(0);
+#pragma unroll
+        for (int i1 = 0; i1 < W; i1++) {
+          const C b = __ldg(row + x1[i1]);
+          sr += b.x * k1[i1];
+          si += b.y * k1[i1];
+        }
+        sr3 += sr * k2[i2];
+        si3 += si * k2[i2];
+      }
+      const T v3 = DIM == 3 ? k3[i3] : T(1);
+      ar += sr3 * v3;
+      ai += si3 * v3;
+    }
+    C out;
+    out.x = ar;
+    out.y = ai;
+    a.c_out[a.perm[j]] = out;
+  }
+}
+
+// ---------------------------------------------------------------- launchers
+
+template <typename T>
+SIParams<T> make_params(const nufft_plan_s *p) {
+  SIParams<T> a;
+  a.sub = p->subprob;
+  a.perm = p->perm;
+  a.g1 = static_cast<const T *>(p->gcoord[0]);
+  a.g2 = static_cast<const T *>(p->gcoord[1]);
+  a.g3 = static_cast<const T *>(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]);
+  a.grid = static_cast<typename Cplx<T>::type *>(p->grid);
+  a.c_in = nullptr;
+  a.c_out = nullptr;
+  a.beta = (T)p->beta;
+  a.n1 = (int)p->n[0];
+  a.n2 = (int)p->n[1];
+  a.n3 = (int)p->n[2];
+  a.m1 = p->m[0];
+  a.m2 = p->m[1];
+  a.m3 = p->m[2];
+  a.nb1 = p->nb[0];
+  a.nb2 = p->nb[1];
+  return a;
+}
+
+inline size_t tile_cells(const nufft_plan_s *p) {
+  const int pad = (p->w + 1) / 2;
+  size_t cells = 1;
+  for (int d = 0; d < p->dim; d++) cells *= (size_t)(p->m[d] + 2 * pad);
+  return cells;
+}
+
+// Kernels that need more than the default 48 KB of dynamic shared memory must
+// opt in before launch.
+template <typename Kern>
+cudaError_t allow_smem(Kern kern, size_t smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <int DIM, typename T, int W>
+cudaError_t spread_w(const nufft_plan_s *p, const void *c) {
+  SIParams<T> a = make_params<T>(p);
+  a.c_in = static_cast<const typename Cplx<T>::type *>(c);
+  const unsigned blocks = (unsigned)p->nsub;
+  if (p->method == NUFFT_METHOD_GM_SORT) {
+    spread_gm_kernel<T, DIM, W><<<blocks, p->threads, 0, p->stream>>>(a);
+    return cudaGetLastError();
+  }
+  const size_t smem = tile_cells(p) * 2 * sizeof(T);
+  cudaError_t e = allow_smem(spread_sm_kernel<T, DIM, W>, smem);
+  if (e != cudaSuccess) return e;
+  spread_sm_kernel<T, DIM, W><<<blocks, p->threads, smem, p->stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DIM, typename T, int W>
+cudaError_t interp_w(const nufft_plan_s *p, void *c) {
+  SIParams<T> a = make_params<T>(p);
+  a.c_out = static_cast<typename Cplx<T>::type *>(c);
+  const unsigned blocks = (unsigned)p->nsub;
+  if (p->method == NUFFT_METHOD_GM_SORT) {
+    interp_gm_kernel<T, DIM, W><<<blocks, p->threads, 0, p->stream>>>(a);
+    return cudaGetLastError();
+  }
+  const size_t smem = tile_cells(p) * 2 * sizeof(T);
+  cudaError_t e = allow_smem(interp_sm_kernel<T, DIM, W>, smem);
+  if (e != cudaSuccess) return e;
+  interp_sm_kernel<T, DIM, W><<<blocks, p->threads, smem, p->stream>>>(a);
+  return cudaGetLastError();
+}
+
+// Dispatch on the kernel width (compile-time in the kernels).
+template <int DIM, typename T>
+cudaError_t launch_spread_t(const nufft_plan_s *p, const void *c) {
+  switch (p->w) {
+    case 2: return spread_w<DIM, T, 2>(p, c);
+    case 3: return spread_w<DIM, T, 3>(p, c);
+    case 4: return spread_w<DIM, T, 4>(p, c);
+    case 5: return spread_w<DIM, T, 5>(p, c);
+    case 6: return spread_w<DIM, T, 6>(p, c);
+    case 7: return spread_w<DIM, T, 7>(p, c);
+    case 8: return spread_w<DIM, T, 8>(p, c);
+    case 9: return spread_w<DIM, T, 9>(p, c);
+    case 10: return spread_w<DIM, T, 10>(p, c);
+    case 11: return spread_w<DIM, T, 11>(p, c);
+    case 12: return spread_w<DIM, T, 12>(p, c);
+    case 13: return spread_w<DIM, T, 13>(p, c);
+    case 14: return spread_w<DIM, T, 14>(p, c);
+    case 15: return spread_w<DIM, T, 15>(p, c);
+    case 16: return spread_w<DIM, T, 16>(p, c);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int DIM, typename T>
+cudaError_t launch_interp_t(const nufft_plan_s *p, void *c) {
+  switch (p->w) {
+    case 2: return interp_w<DIM, T, 2>(p, c);
+    case 3: return interp_w<DIM, T, 3>(p, c);
+    case 4: return interp_w<DIM, T, 4>(p, c);
+    case 5: return interp_w<DIM, T, 5>(p, c);
+    case 6: return interp_w<DIM, T, 6>(p, c);
+    case 7: return interp_w<DIM, T, 7>(p, c);
+    case 8: return interp_w<DIM, T, 8>(p, c);
+    case 9: return interp_w<DIM, T, 9>(p, c);
+    case 10: return interp_w<DIM, T, 10>(p, c);
+    case 11: return interp_w<DIM, T, 11>(p, c);
+    case 12: return interp_w<DIM, T, 12>(p, c);
+    case 13: return interp_w<DIM, T, 13>(p, c);
+    case 14: return interp_w<DIM, T, 14>(p, c);
+    case 15: return interp_w<DIM, T, 15>(p, c);
+    case 16: return interp_w<DIM, T, 16>(p, c);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace nufft

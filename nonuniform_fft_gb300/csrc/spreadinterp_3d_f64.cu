@@ -1,0 +1,7 @@
+// Spreading / interpolation kernels instantiated for 3D, double precision.
+#include "spreadinterp.cuh"
+
+namespace nufft {
+template cudaError_t launch_spread_t<3, double>(const nufft_plan_s *, const void *);
+template cudaError_t launch_interp_t<3, double>(const nufft_plan_s *, void *);
+}  // namespace nufft

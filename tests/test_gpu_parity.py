@@ -1,0 +1,284 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Tolerances (the method's own, see "cuFINUFFT: a load-balanced GPU library for
+general-purpose nonuniform FFTs", Sec. II):
+  * GPU vs the oracle's three-step NUFFT with identical parameters, relative
+    l2: 1e-5 for complex64, 1e-12 for complex128 (only rounding differs);
+  * GPU vs the direct sums of eq. (1) / eq. (3): at most 2 eps, and never
+    more than 25 % above the oracle NUFFT's own error on the same outputs
+    (the method's error is "close to eps": about 3 eps for w = 13 in 3D);
+  * integer setpts results (bin counts, starts, subproblem table): identical
+    to the oracle's counting sort; the order of points inside a bin is not
+    unique, so the permutation is compared bin by bin as a set.
+"""
+import numpy as np
+import pytest
+import torch
+
+import nonuniform_fft_gb300 as nf
+import oracle
+from nonuniform_fft_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+TOL_O2 = {"f32": 1e-5, "f64": 1e-12}
+
+
+def _dtypes(dt):
+    return ("complex64", np.float32, np.complex64) if dt == "f32" else \
+        ("complex128", np.float64, np.complex128)
+
+
+def gpu_transform(ttype, pts, data, N, eps, iflag, dt, opts=None, host=False, plan_out=None):
+    """Run one transform through the C ABI; returns a numpy array (f shaped
+    (N3,) N2, N1 for type 1; c of length M for type 2)."""
+    cname, rdt, cdt = _dtypes(dt)
+    M = len(pts[0])
+    if host:
+        xs = [np.ascontiguousarray(p, dtype=rdt) for p in pts]
+        d = np.ascontiguousarray(data, dtype=cdt)
+        out = np.zeros(tuple(reversed(N)) if ttype == 1 else (M,), dtype=cdt)
+    else:
+        xs = [torch.from_numpy(np.ascontiguousarray(p, dtype=rdt)).to(DEV) for p in pts]
+        d = torch.from_numpy(np.ascontiguousarray(data, dtype=cdt)).to(DEV)
+        out = torch.zeros(tuple(reversed(N)) if ttype == 1 else (M,), dtype=getattr(torch, cname),
+                          device=DEV)
+    with nf.Plan(ttype, N, iflag, eps, cname, **(opts or {})) as plan:
+        plan.setpts(*xs)
+        if ttype == 1:
+            plan.execute(d, out)
+        else:
+            plan.execute(out, d)
+        if plan_out is not None:
+            plan_out.update(plan.info())
+            plan_out["timings"] = plan.timings()
+        torch.cuda.synchronize()
+    return out if host else out.cpu().numpy()
+
+
+def _pts(dim, M, dist, rng, dt):
+    _, rdt, _ = _dtypes(dt)
+    if dist == "uniform":
+        return [rng.uniform(-np.pi, np.pi, M).astype(rdt) for _ in range(dim)]
+    if dist == "cluster":
+        return [(np.mod(rng.normal(0, 0.05, M) + np.pi, 2 * np.pi) - np.pi).astype(rdt)
+                for _ in range(dim)]
+    if dist == "wild":   # far outside [-pi, pi) and on the fold boundaries
+        v = [rng.uniform(-40, 40, M) for _ in range(dim)]
+        for a in v:
+            a[: min(6, M)] = [-np.pi, np.pi, 2 * np.pi, -1e-300, 0.0, 3 * np.pi][: min(6, M)]
+        return [a.astype(rdt) for a in v]
+    raise ValueError(dist)
+
+
+def _cplx(n, rng, dt):
+    _, _, cdt = _dtypes(dt)
+    return (rng.standard_normal(n) + 1j * rng.standard_normal(n)).astype(cdt)
+
+
+def _check_direct(err_gpu, err_o2, eps):
+    bound = max(2 * eps, 1.25 * err_o2)
+    assert err_gpu <= bound, f"GPU vs direct {err_gpu:.3e} > {bound:.3e} (oracle NUFFT {err_o2:.3e})"
+
+
+# ---------------------------------------------------------------- setpts
+
+SORT_CASES = [
+    # dim, N, M, dist, dt, opts
+    (2, (100, 70), 20000, "uniform", "f32", {"msub": 256}),
+    (2, (100, 70), 20000, "cluster", "f32", {"msub": 100}),
+    (2, (64, 64), 5000, "wild", "f64", {}),
+    (3, (20, 24, 36), 30000, "uniform", "f32", {"bin1": 8, "bin2": 8, "bin3": 4, "msub": 128}),
+    (3, (20, 24, 36), 30000, "cluster", "f64", {}),
+    (2, (3, 5), 50, "uniform", "f32", {"bin1": 5, "bin2": 7}),
+]
+
+
+@pytest.mark.parametrize("dim,N,M,dist,dt,opts", SORT_CASES)
+def test_setpts_integer_results_match_oracle(dim, N, M, dist, dt, opts):
+    rng = np.random.default_rng(11)
+    pts = _pts(dim, M, dist, rng, dt)
+    cname, rdt, _ = _dtypes(dt)
+    xs = [torch.from_numpy(p).to(DEV) for p in pts]
+    with nf.Plan(1, N, -1, 1e-6 if dt == "f32" else 1e-12, cname, **opts) as plan:
+        plan.setpts(*xs)
+        info = plan.info()
+        got = plan.sort()
+    n = [info["n1"], info["n2"], info["n3"]][:dim]
+    m = [info["bin1"], info["bin2"], info["bin3"]][:dim]
+    ref = oracle.binsort(pts, n, m, info["msub"])
+    assert info["nbins"] == ref["counts"].size
+    np.testing.assert_array_equal(got["counts"], ref["counts"])
+    np.testing.assert_array_equal(got["starts"], ref["starts"])
+    np.testing.assert_array_equal(got["subproblems"], ref["subproblems"])
+    for lo, cnt in zip(ref["starts"], ref["counts"]):
+        np.testing.assert_array_equal(np.sort(got["perm"][lo:lo + cnt]), ref["perm"][lo:lo + cnt])
+
+
+# ---------------------------------------------------------------- transforms
+
+T_CASES = []
+for _dim, _N in ((2, (100, 70)), (3, (20, 24, 36))):
+    for _dt, _epss in (("f32", (1e-2, 1e-5, 1e-6)), ("f64", (1e-3, 1e-9, 1e-12))):
+        for _eps in _epss:
+            T_CASES.append((_dim, _N, _dt, _eps))
+
+
+@pytest.mark.parametrize("method", [nf.METHOD_SM, nf.METHOD_GM_SORT])
+@pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
+def test_type1_matches_oracle(dim, N, dt, eps, method):
+    rng = np.random.default_rng(21)
+    M = 20000
+    pts = _pts(dim, M, "uniform", rng, dt)
+    c = _cplx(M, rng, dt)
+    for iflag in (-1, 1):
+        f = gpu_transform(1, pts, c, N, eps, iflag, dt, {"method": method, "msub": 300})
+        o2 = oracle.nufft_type1(pts, c, N, eps, iflag)
+        o1 = oracle.direct_type1(pts, c, N, iflag)
+        e = oracle.rel_l2(f, o2)
+        assert e <= TOL_O2[dt], f"GPU vs oracle NUFFT {e:.3e}"
+        _check_direct(oracle.rel_l2(f, o1), oracle.rel_l2(o2, o1), eps)
+
+
+@pytest.mark.parametrize("method", [nf.METHOD_SM, nf.METHOD_GM_SORT])
+@pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
+def test_type2_matches_oracle(dim, N, dt, eps, method):
+    rng = np.random.default_rng(22)
+    M = 20000
+    pts = _pts(dim, M, "uniform", rng, dt)
+    f = _cplx(int(np.prod(N)), rng, dt)
+    for iflag in (-1, 1):
+        c = gpu_transform(2, pts, f, N, eps, iflag, dt, {"method": method, "msub": 300})
+        o2 = oracle.nufft_type2(pts, f, N, eps, iflag)
+        tg = np.arange(0, M, 7)
+        o1 = oracle.direct_type2(pts, f, N, iflag, targets=tg)
+        e = oracle.rel_l2(c, o2)
+        assert e <= TOL_O2[dt], f"GPU vs oracle NUFFT {e:.3e}"
+        _check_direct(oracle.rel_l2(c[tg], o1), oracle.rel_l2(o2[tg], o1), eps)
+
+
+@pytest.mark.parametrize("dim,N,dt", [(2, (48, 40), "f32"), (3, (12, 10, 16), "f64")])
+def test_adjoint_identity_on_gpu(dim, N, dt):
+    """<T1_s(c), f> = <c, T2_-s(f)> holds to rounding for the GPU transforms."""
+    rng = np.random.default_rng(5)
+    M = 5000
+    pts = _pts(dim, M, "uniform", rng, dt)
+    c = _cplx(M, rng, dt).astype(np.complex128)
+    f = _cplx(int(np.prod(N)), rng, dt).astype(np.complex128)
+    for s in (-1, 1):
+        t1 = gpu_transform(1, pts, c, N, 1e-6 if dt == "f32" else 1e-12, s, dt).astype(np.complex128)
+        t2 = gpu_transform(2, pts, f, N, 1e-6 if dt == "f32" else 1e-12, -s, dt).astype(np.complex128)
+        lhs = np.vdot(t1.ravel(), f)
+        rhs = np.vdot(c, t2)
+        tol = 1e-5 if dt == "f32" else 1e-12
+        assert abs(lhs - rhs) <= tol * abs(lhs)
+
+
+def test_clustered_points_single_bin():
+    """Every point in one fine cell: one bin, many subproblems (SM step 1
+    load balancing), heavy atomic contention."""
+    rng = np.random.default_rng(9)
+    M = 50000
+    h = 2 * np.pi / 256
+    pts = [(0.3 + rng.uniform(0, h, M)).astype(np.float32) for _ in range(2)]
+    c = _cplx(M, rng, "f32")
+    info = {}
+    f = gpu_transform(1, pts, c, (128, 128), 1e-5, -1, "f32", plan_out=info)
+    assert info["nsub"] >= M // 1024
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, (128, 128), 1e-5, -1)) <= 1e-5
+
+
+@pytest.mark.parametrize("N", [(1, 1), (2, 3), (1, 4, 2)])
+def test_tiny_mode_counts(N):
+    """Fine grid of 2w points per dimension: the padded tile wraps onto itself."""
+    rng = np.random.default_rng(4)
+    pts = _pts(len(N), 300, "uniform", rng, "f64")
+    c = _cplx(300, rng, "f64")
+    f = gpu_transform(1, pts, c, N, 1e-9, 1, "f64")
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, 1e-9, 1)) <= 1e-12
+    fk = _cplx(int(np.prod(N)), rng, "f64")
+    c2 = gpu_transform(2, pts, fk, N, 1e-9, -1, "f64")
+    assert oracle.rel_l2(c2, oracle.nufft_type2(pts, fk, N, 1e-9, -1)) <= 1e-12
+
+
+def test_wild_coordinates_fold():
+    rng = np.random.default_rng(6)
+    pts = _pts(2, 4000, "wild", rng, "f64")
+    c = _cplx(4000, rng, "f64")
+    f = gpu_transform(1, pts, c, (30, 22), 1e-12, -1, "f64")
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, (30, 22), 1e-12, -1)) <= 1e-12
+
+
+def test_host_pointers_match_device_pointers():
+    rng = np.random.default_rng(8)
+    pts = _pts(2, 3000, "uniform", rng, "f32")
+    c = _cplx(3000, rng, "f32")
+    fd = gpu_transform(1, pts, c, (40, 24), 1e-5, -1, "f32")
+    fh = gpu_transform(1, pts, c, (40, 24), 1e-5, -1, "f32", host=True)
+    assert oracle.rel_l2(fh, fd) <= 1e-6
+    fk = _cplx(40 * 24, rng, "f32")
+    cd = gpu_transform(2, pts, fk, (40, 24), 1e-5, 1, "f32")
+    ch = gpu_transform(2, pts, fk, (40, 24), 1e-5, 1, "f32", host=True)
+    assert oracle.rel_l2(ch, cd) <= 1e-6
+
+
+def test_zero_points():
+    f = gpu_transform(1, [np.zeros(0), np.zeros(0)], np.zeros(0), (16, 8), 1e-6, -1, "f32")
+    assert f.shape == (8, 16) and np.all(f == 0)
+    c = gpu_transform(2, [np.zeros(0), np.zeros(0)], np.ones(128), (16, 8), 1e-6, 1, "f32")
+    assert c.shape == (0,)
+
+
+def test_single_point_closed_form():
+    N = (33, 20)
+    x0 = [np.array([-np.pi]), np.array([1.234])]
+    f = gpu_transform(1, x0, np.ones(1), N, 1e-12, -1, "f64")
+    k1 = np.arange(-(N[0] // 2), N[0] - N[0] // 2)[None, :]
+    k2 = np.arange(-(N[1] // 2), N[1] - N[1] // 2)[:, None]
+    ref = np.exp(-1j * (k1 * x0[0][0] + k2 * x0[1][0]))
+    assert oracle.rel_l2(f, ref) <= 20e-12
+
+
+def test_errors_reported():
+    xs = [torch.tensor([0.1, float("nan")], device=DEV), torch.tensor([0.0, 0.2], device=DEV)]
+    plan = nf.Plan(1, (8, 8), -1, 1e-5, "complex64")
+    try:
+        with pytest.raises(nf.NufftError) as ei:
+            plan.execute(torch.zeros(2, dtype=torch.complex64, device=DEV),
+                         torch.zeros(64, dtype=torch.complex64, device=DEV))
+        assert ei.value.code == nf.ERR_NO_POINTS
+        with pytest.raises(nf.NufftError) as ei:
+            plan.setpts(*xs)
+        assert ei.value.code == nf.ERR_BAD_POINTS
+        with pytest.raises(nf.NufftError) as ei:
+            plan.set_opt("no_such_key", 1)
+        assert ei.value.code == nf.ERR_BAD_OPT
+        with pytest.raises(nf.NufftError) as ei:
+            plan.set_opt("threads", 33)
+        assert ei.value.code == nf.ERR_BAD_OPT
+        # too-large bins for shared memory are refused at setpts
+        big = [torch.zeros(4, device=DEV), torch.zeros(4, device=DEV)]
+        p2 = nf.Plan(1, (2048, 2048), -1, 1e-5, "complex64", bin1=1024, bin2=1024)
+        with pytest.raises(nf.NufftError) as ei:
+            p2.setpts(*big)
+        assert ei.value.code == nf.ERR_BAD_OPT
+        p2.close()
+    finally:
+        plan.close()
+
+
+def test_plan_reuse_new_strengths_and_points():
+    """One plan, several setpts and executes (Sec. I-A 'plan, setup, execute')."""
+    rng = np.random.default_rng(12)
+    N = (50, 36)
+    with nf.Plan(1, N, -1, 1e-6, "complex64") as plan:
+        for M in (5000, 20000, 700):
+            pts = _pts(2, M, "uniform", rng, "f32")
+            plan.setpts(*[torch.from_numpy(p).to(DEV) for p in pts])
+            for _ in range(2):
+                c = _cplx(M, rng, "f32")
+                f = torch.zeros(N[1], N[0], dtype=torch.complex64, device=DEV)
+                plan.execute(torch.from_numpy(c).to(DEV), f)
+                ref = oracle.nufft_type1(pts, c, N, 1e-6, -1)
+                assert oracle.rel_l2(f.cpu().numpy(), ref) <= 1e-5
