@@ -62,6 +62,22 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(value: float, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_step: int, steps: int, t_max_s: float) -> float:
+    """Whole-job throughput: units every rank processed / slowest rank's time."""
+    return world * units_per_step * steps / t_max_s
+
+
 def algorithmic_bytes(wl: W.Workload, n) -> dict:
     """Minimum bytes each kernel must move per launch (one transform):
     coordinates (d reals), one complex strength / result and one 4-byte
@@ -264,13 +280,9 @@ def run_ours(args, wl):
     if world > 1:
         dist.barrier()
     total_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1))
-    t_max = total_ms
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = reduce_max(total_ms, dev)
     pts_per_step = 2 * wl.M
-    value = world * pts_per_step * args.steps / (t_max / 1e3)
+    value = job_throughput(world, pts_per_step, args.steps, t_max / 1e3)
 
     # roofline of the dominant kernel (per-launch averages over the timed region)
     K = args.steps
@@ -304,14 +316,10 @@ def run_ours(args, wl):
         for _ in range(e2e_steps):
             p1.execute(hc, hf_out)        # host c in, host f out (synchronous)
             p2.execute(hc_out, hf)        # host f in, host c out (synchronous)
-        el = time.perf_counter() - t0
-        if world > 1:
-            t = torch.tensor([el], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            el = float(t.item())
+        el = reduce_max(time.perf_counter() - t0, dev)
         cb = hc.element_size()
         modes = int(np.prod(N))
-        e2e = {"value": world * pts_per_step * e2e_steps / el, "unit": "NU points/s",
+        e2e = {"value": job_throughput(world, pts_per_step, e2e_steps, el), "unit": "NU points/s",
                "h2d_bytes_per_step": wl.M * cb + modes * cb,
                "d2h_bytes_per_step": modes * cb + wl.M * cb}
 
