@@ -175,6 +175,42 @@ int nufft_get_info(nufft_plan_t plan, int64_t *info, int n);
 int nufft_get_sort(nufft_plan_t plan, int32_t *counts, int32_t *starts, int32_t *perm,
                    int32_t *subprob);
 
+/*
+ * Bin sort without any memory allocation.  The paper has no counterpart: this
+ * entry point exists for callers that cannot call cudaMalloc.  Examples are
+ * code running while a stream is being captured into a CUDA graph, where
+ * allocation calls are not allowed; hosts whose device memory is entirely
+ * reserved by their own pool allocator; and real-time loops that must not pay
+ * allocation latency or risk out-of-memory in the middle of a run.
+ *
+ * It computes what nufft_setpts computes for its counts and permutation: each
+ * point's fine-grid cell and bin (bins of bins[i] cells, x fastest, smaller at
+ * the far edge), the number of points per bin, and the permutation listing
+ * the points of bin 0, then bin 1, ...  The order inside a bin is
+ * unspecified.
+ *   dim, dtype    2 or 3; 0 = float coordinates, 1 = double.
+ *   M             number of points, 0 <= M <= 1,048,576.
+ *   x, y, z       DEVICE arrays of M coordinates (z unused in 2D), read mod 2 pi.
+ *   n_fine, bins  HOST arrays of dim fine-grid sizes and bin sizes (bins are
+ *                 clamped to the grid).  At most 65,536 bins in total.
+ *   counts        DEVICE output, one int32 per bin (overwritten).
+ *   perm          DEVICE output, M int32 (overwritten).
+ *   cuda_stream   stream to run on (NULL: legacy default stream).
+ * Scratch: a fixed 8.3 MB array in the library's device memory, present on
+ * every GPU that loads the library until the process exits.  The first call on
+ * each device looks up that array's device address (once, with the device
+ * current); make that first call before any stream capture.  All calls share
+ * the one array: calls that overlap on the GPU (different streams, or several
+ * host threads) race and must be serialised by the caller.  The call returns
+ * after the sort has finished (it waits for the stream).
+ * Calls no cudaMalloc, cudaFree or allocating library routine.
+ * Errors: BAD_ARG, TOO_LARGE (M or the bin count above the limits),
+ * BAD_POINTS (a NaN/Inf coordinate), CUDA.
+ */
+int nufft_binsort_noalloc(int dim, int dtype, int64_t M, const void *x, const void *y,
+                          const void *z, const int64_t *n_fine, const int64_t *bins,
+                          int32_t *counts, int32_t *perm, void *cuda_stream);
+
 /* Static description of an error code. */
 const char *nufft_strerror(int code);
 

@@ -13,6 +13,7 @@
 // in double precision with explicitly rounded operations (no fused
 // multiply-add): g = n * frac(x / (2 pi)), node l at l h (eq. (7)).
 #include <cmath>
+#include <mutex>
 
 #include "nufft_internal.cuh"
 
@@ -240,3 +241,124 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
 }
 
 }  // namespace nufft
+
+namespace nufft {
+// ===================================================================== no-allocation bin sort
+//
+// nufft_binsort_noalloc: the bin sort above (count, scan, permute) for callers
+// that must not allocate device memory.  Its scratch (each point's bin and
+// rank, the bin starts, the scan partials, the error flag) lives in the
+// file-scope array below instead of cudaMalloc'd buffers.
+
+namespace {
+
+constexpr int64_t kNoAllocMaxPoints = int64_t(1) << 20;  // 1,048,576 points
+constexpr int64_t kNoAllocMaxBins = int64_t(1) << 16;    // 65,536 bins
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+constexpr size_t kOffBinOf = 0;
+constexpr size_t kOffRankOf = align256(kOffBinOf + sizeof(int32_t) * kNoAllocMaxPoints);
+constexpr size_t kOffStarts = align256(kOffRankOf + sizeof(int32_t) * kNoAllocMaxPoints);
+constexpr size_t kOffScan = align256(kOffStarts + sizeof(int32_t) * (kNoAllocMaxBins + 1));
+constexpr size_t kScanInts = (kNoAllocMaxBins + 1 + 4095) / 4096 + 1;  // scan_scratch_len bound
+constexpr size_t kOffFlag = align256(kOffScan + sizeof(int32_t) * kScanInts);
+constexpr size_t kNoAllocBytes = align256(kOffFlag + sizeof(int));  // about 8.3 MB
+
+// Held by every GPU that loads the library, until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned char *g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the symbol is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(unsigned char **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NUFFT_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return NUFFT_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = static_cast<unsigned char *>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return NUFFT_OK;
+}
+
+// Writes only the permutation: slot starts[bin] + rank <- caller index.
+__global__ void permute_only_kernel(int64_t M, const int32_t *starts, const int32_t *bin_of,
+                                    const int32_t *rank_of, int32_t *perm) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= M) return;
+  perm[starts[bin_of[j]] + rank_of[j]] = (int32_t)j;
+}
+
+}  // namespace
+}  // namespace nufft
+
+using nufft::PointsIn;
+
+extern "C" int nufft_binsort_noalloc(int dim, int dtype, int64_t M, const void *x, const void *y,
+                                     const void *z, const int64_t *n_fine, const int64_t *bins,
+                                     int32_t *counts, int32_t *perm, void *cuda_stream) {
+  if ((dim != 2 && dim != 3) || (dtype != 0 && dtype != 1) || M < 0 || !n_fine || !bins ||
+      !counts || (M > 0 && (!x || !y || (dim == 3 && !z) || !perm)))
+    return NUFFT_ERR_BAD_ARG;
+  PointsIn a;
+  int64_t nbins = 1;
+  for (int d = 0; d < 3; d++) {
+    const int64_t n = d < dim ? n_fine[d] : 1, m = d < dim ? bins[d] : 1;
+    if (n < 1 || m < 1 || n > (int64_t(1) << 30)) return NUFFT_ERR_BAD_ARG;
+    a.n[d] = (int)n;
+    a.m[d] = (int)(m < n ? m : n);
+    a.nb[d] = (int)((n + a.m[d] - 1) / a.m[d]);
+    nbins *= a.nb[d];
+  }
+  if (M > nufft::kNoAllocMaxPoints || nbins > nufft::kNoAllocMaxBins) return NUFFT_ERR_TOO_LARGE;
+  unsigned char *base = nullptr;
+  int rc = nufft::noalloc_scratch(&base);
+  if (rc) return rc;
+  using namespace nufft;
+  int32_t *bin_of = reinterpret_cast<int32_t *>(base + kOffBinOf);
+  int32_t *rank_of = reinterpret_cast<int32_t *>(base + kOffRankOf);
+  int32_t *starts = reinterpret_cast<int32_t *>(base + kOffStarts);
+  int32_t *scan = reinterpret_cast<int32_t *>(base + kOffScan);
+  int *flag = reinterpret_cast<int *>(base + kOffFlag);
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+
+  a.x[0] = x;
+  a.x[1] = y;
+  a.x[2] = dim == 3 ? z : x;
+  a.M = M;
+  a.dim = dim;
+  a.is_double = dtype;
+  a.inv_two_pi = 1.0 / (2.0 * 3.14159265358979323846);
+  // the shared scratch keeps the previous call's contents: clear what sums
+  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)nbins, s) != cudaSuccess ||
+      cudaMemsetAsync(flag, 0, sizeof(int), s) != cudaSuccess)
+    return NUFFT_ERR_CUDA;
+  const int threads = 256;
+  const unsigned blocks = (unsigned)((M + threads - 1) / threads);
+  if (M > 0) {
+    if (dtype == 0)
+      nufft::bin_count_kernel<float><<<blocks, threads, 0, s>>>(a, counts, bin_of, rank_of, flag);
+    else
+      nufft::bin_count_kernel<double><<<blocks, threads, 0, s>>>(a, counts, bin_of, rank_of, flag);
+    if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+  if (nufft::exclusive_scan(counts, starts, nbins, scan, s) != cudaSuccess) return NUFFT_ERR_CUDA;
+  if (M > 0) {
+    nufft::permute_only_kernel<<<blocks, threads, 0, s>>>(M, starts, bin_of, rank_of, perm);
+    if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+  int host_flag = 0;
+  if (cudaMemcpyAsync(&host_flag, flag, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NUFFT_ERR_CUDA;
+  return host_flag ? NUFFT_ERR_BAD_POINTS : NUFFT_OK;
+}
