@@ -45,6 +45,7 @@ struct nufft_plan_s {
   int opt_bin[3] = {0, 0, 0};  // 0: default
   int opt_msub = 0;            // 0: default
   int opt_threads = 0;         // 0: default
+  int opt_regtile_cols = 0;    // 0: default
 
   // --- resolved at setpts ------------------------------------------------
   int method = NUFFT_METHOD_SM;
@@ -52,6 +53,7 @@ struct nufft_plan_s {
   int nb[3] = {1, 1, 1};
   int msub = 1024;
   int threads = 256;
+  int regtile_cols = 4;        // tile columns per lane of the register-tile spreader
   int64_t nbins = 0;
   int64_t nsub = 0;
   int64_t M = 0;
@@ -64,11 +66,14 @@ struct nufft_plan_s {
   int32_t *bin_starts = nullptr;   // nbins + 1 (last entry: M)
   int32_t *sub_counts = nullptr;   // nbins + 1
   int32_t *sub_starts = nullptr;   // nbins + 1
-  int32_t *scan_scratch = nullptr; // block partials of the scan
   int64_t cap_bins = 0;
+  int32_t *cell_counts = nullptr;  // nbins * cells_per_bin + 1 (cell-level counting sort)
+  int32_t *cell_starts = nullptr;  // same length: first sorted slot of each (bin, cell)
+  int32_t *scan_scratch = nullptr; // block partials of the scans
+  int64_t cap_keys = 0;
   int32_t *perm = nullptr;         // M: sorted slot -> user index
   void *gcoord[3] = {nullptr, nullptr, nullptr};  // M bin-relative grid coordinates
-  int32_t *bin_of = nullptr;       // M (setpts scratch)
+  int32_t *bin_of = nullptr;       // M (setpts scratch: each point's cell key)
   int32_t *rank_of = nullptr;      // M (setpts scratch)
   int64_t cap_pts = 0;
   nufft::Subproblem *subprob = nullptr;
@@ -106,6 +111,12 @@ template <int DIM, typename T>
 cudaError_t launch_spread_t(const nufft_plan_s *p, const void *c);
 template <int DIM, typename T>
 cudaError_t launch_interp_t(const nufft_plan_s *p, void *c);
+
+// Register-tile 2D spreader (spread_regtile.cuh), instantiated in
+// spread_regtile_{f32,f64}.cu, and the bin size it is built for.
+template <typename T>
+cudaError_t launch_spread_regtile2d(const nufft_plan_s *p, const void *c);
+void regtile2d_bins(int w, int cols, int *m1, int *m2);
 
 // deconv.cu: type 1 correction + truncation, type 2 correction + padding.
 cudaError_t launch_deconvolve(const nufft_plan_s *p, void *f);

@@ -130,13 +130,15 @@ int grow_buffer(void **buf, int64_t *cap, int64_t bytes) {
   return NUFFT_OK;
 }
 
-// Default bin sizes (Sec. III-A Remark 1 gives 32 x 32 in 2D): in 3D the
-// largest bins, halving the longest side, whose padded tile fits the budget.
+// Default bin sizes.  2D: the padded bin of the interpolator is 32 x 32
+// cells (bins 32 - 2 ceil(w/2) square; Sec. III-A Remark 1 found 32 x 32 bins
+// best on its GPU).  3D: the largest bins, halving the longest side, whose
+// padded tile fits the shared-memory budget.
 void default_bins(const nufft_plan_s *p, int m[3]) {
   const int pad = (p->w + 1) / 2;
   const size_t cs = 2 * real_size(p);
   if (p->dim == 2) {
-    m[0] = m[1] = 32;
+    m[0] = m[1] = 32 - 2 * pad;
     m[2] = 1;
   } else {
     m[0] = m[1] = 16;
@@ -171,6 +173,8 @@ void release(nufft_plan_s *p) {
   cudaFree(p->sub_counts);
   cudaFree(p->sub_starts);
   cudaFree(p->scan_scratch);
+  cudaFree(p->cell_counts);
+  cudaFree(p->cell_starts);
   cudaFree(p->perm);
   cudaFree(p->bin_of);
   cudaFree(p->rank_of);
@@ -300,7 +304,9 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
   if (!std::isfinite(value) || value != std::floor(value)) return NUFFT_ERR_BAD_OPT;
   const int64_t v = (int64_t)value;
   if (!std::strcmp(key, "method")) {
-    if (v != NUFFT_METHOD_AUTO && v != NUFFT_METHOD_SM && v != NUFFT_METHOD_GM_SORT) return NUFFT_ERR_BAD_OPT;
+    if (v != NUFFT_METHOD_AUTO && v != NUFFT_METHOD_SM && v != NUFFT_METHOD_GM_SORT &&
+        v != NUFFT_METHOD_REGTILE)
+      return NUFFT_ERR_BAD_OPT;
     p->opt_method = (int)v;
   } else if (!std::strcmp(key, "bin1") || !std::strcmp(key, "bin2") || !std::strcmp(key, "bin3")) {
     if (v < 0 || v > 4096) return NUFFT_ERR_BAD_OPT;
@@ -308,6 +314,9 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
   } else if (!std::strcmp(key, "msub")) {
     if (v < 0 || v > (int64_t(1) << 24)) return NUFFT_ERR_BAD_OPT;
     p->opt_msub = (int)v;
+  } else if (!std::strcmp(key, "regtile_cols")) {
+    if (v != 0 && v != 1 && v != 2 && v != 4) return NUFFT_ERR_BAD_OPT;
+    p->opt_regtile_cols = (int)v;
   } else if (!std::strcmp(key, "threads")) {
     if (v != 0 && (v < 32 || v > 1024 || v % 32)) return NUFFT_ERR_BAD_OPT;
     p->opt_threads = (int)v;
@@ -324,11 +333,17 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   if (cudaSetDevice(p->device) != cudaSuccess) return NUFFT_ERR_CUDA;
 
   // resolve options
-  p->method = p->opt_method == NUFFT_METHOD_AUTO ? NUFFT_METHOD_SM : p->opt_method;
+  p->method = p->opt_method;
+  if (p->method == NUFFT_METHOD_AUTO)
+    p->method = p->dim == 2 && p->type == 1 ? NUFFT_METHOD_REGTILE : NUFFT_METHOD_SM;
+  if (p->method == NUFFT_METHOD_REGTILE && p->dim != 2) return NUFFT_ERR_BAD_OPT;
   int m[3];
   default_bins(p, m);
-  for (int d = 0; d < 3; d++) {
+  for (int d = 0; d < 3; d++)
     if (d < p->dim && p->opt_bin[d] > 0) m[d] = p->opt_bin[d];
+  p->regtile_cols = p->opt_regtile_cols > 0 ? p->opt_regtile_cols : 1;
+  if (p->method == NUFFT_METHOD_REGTILE) nufft::regtile2d_bins(p->w, p->regtile_cols, &m[0], &m[1]);
+  for (int d = 0; d < 3; d++) {
     if (d >= p->dim) m[d] = 1;
     if (m[d] > p->n[d]) m[d] = (int)p->n[d];
   }
@@ -342,7 +357,10 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
     p->nb[d] = (int)((p->n[d] + m[d] - 1) / m[d]);
     p->nbins *= p->nb[d];
   }
-  p->msub = p->opt_msub > 0 ? p->opt_msub : 1024;
+  p->msub = p->opt_msub > 0 ? p->opt_msub
+                            : (p->method == NUFFT_METHOD_REGTILE ? 512 : (p->type == 2 ? 2048 : 1024));
+  // the cell-level sort indexes (bin, cell) pairs with int32
+  if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
   p->threads = p->opt_threads > 0 ? p->opt_threads : 256;
   p->M = M;
 
@@ -416,6 +434,9 @@ int nufft_execute(nufft_plan_t p, void *c, void *f) {
   };
   auto spread = [&]() -> cudaError_t {
     if (p->nsub == 0) return cudaSuccess;
+    if (p->method == NUFFT_METHOD_REGTILE)
+      return p->dtype == 0 ? nufft::launch_spread_regtile2d<float>(p, dc)
+                           : nufft::launch_spread_regtile2d<double>(p, dc);
     if (p->dim == 2)
       return p->dtype == 0 ? nufft::launch_spread_t<2, float>(p, dc) : nufft::launch_spread_t<2, double>(p, dc);
     return p->dtype == 0 ? nufft::launch_spread_t<3, float>(p, dc) : nufft::launch_spread_t<3, double>(p, dc);

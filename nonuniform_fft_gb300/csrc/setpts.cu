@@ -87,6 +87,69 @@ __global__ void permute_kernel(PointsIn a, const int32_t *starts, const int32_t 
   }
 }
 
+// Cell-level key of a point: its bin, then its cell inside the bin (x fastest).
+// Sorting by this key orders the points bin by bin (as Sec. III-A) and, inside
+// each bin, cell by cell, so a bin's points of one fine-grid row (and one x
+// range of that row) form a contiguous run.
+template <typename T>
+__global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, int32_t *rank_of,
+                                  int *flag) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= a.M) return;
+  bool bad = false;
+  int bin = 0, stride = 1, local = 0, lstride = 1;
+  for (int d = 0; d < a.dim; d++) {
+    double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
+    int cell = (int)floor(g);
+    if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
+    const int b = cell / a.m[d];
+    bin += b * stride;
+    stride *= a.nb[d];
+    local += (cell - b * a.m[d]) * lstride;
+    lstride *= a.m[d];
+  }
+  if (bad) atomicOr(flag, 1);
+  const int32_t key = bin * lstride + local;
+  key_of[j] = key;
+  rank_of[j] = atomicAdd(&counts[key], 1);
+}
+
+__device__ __forceinline__ float below(float v) { return nextafterf(v, 0.0f); }
+__device__ __forceinline__ double below(double v) { return ::nextafter(v, 0.0); }
+
+// Sorted slot of each point; its bin-relative coordinate, rounded to T but
+// never up to the next cell (floor(g) stays the point's cell).
+template <typename T>
+__global__ void cell_permute_kernel(PointsIn a, const int32_t *starts, const int32_t *key_of,
+                                    const int32_t *rank_of, int32_t *perm, T *g0, T *g1, T *g2) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= a.M) return;
+  const int32_t pos = starts[key_of[j]] + rank_of[j];
+  perm[pos] = (int32_t)j;
+  T *out[3] = {g0, g1, g2};
+  bool bad = false;
+  for (int d = 0; d < a.dim; d++) {
+    double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
+    int cell = (int)floor(g);
+    if (cell >= a.n[d]) cell = a.n[d] - 1;
+    const int cell_rel = cell - (cell / a.m[d]) * a.m[d];
+    const double rel = g - (double)((cell / a.m[d]) * a.m[d]);  // exact
+    T v = (T)rel;
+    if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
+    out[d][pos] = v;
+  }
+}
+
+// Bin counts and starts from the cell starts (cpb cells per bin).
+__global__ void bins_from_cells_kernel(const int32_t *cell_starts, int64_t nbins, int64_t cpb,
+                                       int32_t *counts, int32_t *starts) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b > nbins) return;
+  const int32_t s0 = cell_starts[b * cpb];
+  starts[b] = s0;
+  if (b < nbins) counts[b] = cell_starts[(b + 1) * cpb] - s0;
+}
+
 __global__ void sub_count_kernel(const int32_t *counts, int64_t nbins, int msub, int32_t *nsub) {
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nbins) return;
@@ -134,6 +197,8 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
   const int64_t M = p->M;
   cudaStream_t s = p->stream;
   const size_t rs = real_size(p);
+  const int64_t cpb = (int64_t)p->m[0] * p->m[1] * p->m[2];  // cells per bin
+  const int64_t nkeys = p->nbins * cpb;
 
   // --- storage (grown, never shrunk) --------------------------------------
   if (p->nbins + 1 > p->cap_bins || !p->bin_counts) {
@@ -141,18 +206,29 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     cudaFree(p->bin_starts);
     cudaFree(p->sub_counts);
     cudaFree(p->sub_starts);
-    cudaFree(p->scan_scratch);
-    p->bin_counts = p->bin_starts = p->sub_counts = p->sub_starts = p->scan_scratch = nullptr;
+    p->bin_counts = p->bin_starts = p->sub_counts = p->sub_starts = nullptr;
     p->cap_bins = 0;
     const size_t nb = (size_t)(p->nbins + 1) * sizeof(int32_t);
     if (cudaMalloc((void **)&p->bin_counts, nb) != cudaSuccess ||
         cudaMalloc((void **)&p->bin_starts, nb) != cudaSuccess ||
         cudaMalloc((void **)&p->sub_counts, nb) != cudaSuccess ||
-        cudaMalloc((void **)&p->sub_starts, nb) != cudaSuccess ||
-        cudaMalloc((void **)&p->scan_scratch,
-                   (size_t)scan_scratch_len(p->nbins + 1) * sizeof(int32_t)) != cudaSuccess)
+        cudaMalloc((void **)&p->sub_starts, nb) != cudaSuccess)
       return NUFFT_ERR_ALLOC;
     p->cap_bins = p->nbins + 1;
+  }
+  if (nkeys + 1 > p->cap_keys || !p->cell_counts) {
+    cudaFree(p->cell_counts);
+    cudaFree(p->cell_starts);
+    cudaFree(p->scan_scratch);
+    p->cell_counts = p->cell_starts = p->scan_scratch = nullptr;
+    p->cap_keys = 0;
+    const size_t nk = (size_t)(nkeys + 1) * sizeof(int32_t);
+    if (cudaMalloc((void **)&p->cell_counts, nk) != cudaSuccess ||
+        cudaMalloc((void **)&p->cell_starts, nk) != cudaSuccess ||
+        cudaMalloc((void **)&p->scan_scratch,
+                   (size_t)scan_scratch_len(nkeys + 1) * sizeof(int32_t)) != cudaSuccess)
+      return NUFFT_ERR_ALLOC;
+    p->cap_keys = nkeys + 1;
   }
   if (M > p->cap_pts || !p->perm) {
     cudaFree(p->perm);
@@ -173,7 +249,7 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
   }
   if (!p->flag && cudaMalloc((void **)&p->flag, sizeof(int)) != cudaSuccess) return NUFFT_ERR_ALLOC;
 
-  // --- 1. bins and counts ------------------------------------------------
+  // --- 1. cells, bins and counts ------------------------------------------
   PointsIn a;
   a.x[0] = x;
   a.x[1] = y;
@@ -187,38 +263,41 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     a.m[d] = p->m[d];
     a.nb[d] = p->nb[d];
   }
-  if (cudaMemsetAsync(p->bin_counts, 0, (size_t)(p->nbins + 1) * 4, s) != cudaSuccess ||
+  if (cudaMemsetAsync(p->cell_counts, 0, (size_t)(nkeys + 1) * 4, s) != cudaSuccess ||
       cudaMemsetAsync(p->flag, 0, sizeof(int), s) != cudaSuccess)
     return NUFFT_ERR_CUDA;
   const int threads = 256;
   const unsigned blocks_pts = (unsigned)((M + threads - 1) / threads);
   if (M > 0) {
     if (p->dtype == 0)
-      bin_count_kernel<float><<<blocks_pts, threads, 0, s>>>(a, p->bin_counts, p->bin_of, p->rank_of, p->flag);
+      cell_count_kernel<float><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag);
     else
-      bin_count_kernel<double><<<blocks_pts, threads, 0, s>>>(a, p->bin_counts, p->bin_of, p->rank_of, p->flag);
+      cell_count_kernel<double><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
-  // --- 2. bin starts -------------------------------------------------------
-  if (exclusive_scan(p->bin_counts, p->bin_starts, p->nbins, p->scan_scratch, s) != cudaSuccess)
+  // --- 2. cell starts (bin starts are every cpb-th entry) -----------------
+  if (exclusive_scan(p->cell_counts, p->cell_starts, nkeys, p->scan_scratch, s) != cudaSuccess)
     return NUFFT_ERR_CUDA;
+  const unsigned blocks_bins = (unsigned)((p->nbins + 1 + threads - 1) / threads);
+  bins_from_cells_kernel<<<blocks_bins, threads, 0, s>>>(p->cell_starts, p->nbins, cpb,
+                                                         p->bin_counts, p->bin_starts);
+  if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
 
   // --- 3. permutation and sorted coordinates ------------------------------
   if (M > 0) {
     if (p->dtype == 0)
-      permute_kernel<float><<<blocks_pts, threads, 0, s>>>(
-          a, p->bin_starts, p->bin_of, p->rank_of, p->perm, (float *)p->gcoord[0],
+      cell_permute_kernel<float><<<blocks_pts, threads, 0, s>>>(
+          a, p->cell_starts, p->bin_of, p->rank_of, p->perm, (float *)p->gcoord[0],
           (float *)p->gcoord[1], (float *)(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]));
     else
-      permute_kernel<double><<<blocks_pts, threads, 0, s>>>(
-          a, p->bin_starts, p->bin_of, p->rank_of, p->perm, (double *)p->gcoord[0],
+      cell_permute_kernel<double><<<blocks_pts, threads, 0, s>>>(
+          a, p->cell_starts, p->bin_of, p->rank_of, p->perm, (double *)p->gcoord[0],
           (double *)p->gcoord[1], (double *)(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]));
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
   // --- 4. subproblems ------------------------------------------------------
-  const unsigned blocks_bins = (unsigned)((p->nbins + threads - 1) / threads);
   sub_count_kernel<<<blocks_bins, threads, 0, s>>>(p->bin_counts, p->nbins, p->msub, p->sub_counts);
   if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   if (exclusive_scan(p->sub_counts, p->sub_starts, p->nbins, p->scan_scratch, s) != cudaSuccess)

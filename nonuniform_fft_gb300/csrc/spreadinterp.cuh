@@ -29,28 +29,93 @@ template <typename T> struct Cplx;
 template <> struct Cplx<float> { using type = float2; };
 template <> struct Cplx<double> { using type = double2; };
 
-__device__ __forceinline__ float es_exp(float v) { return expf(v); }
-__device__ __forceinline__ double es_exp(double v) { return exp(v); }
-__device__ __forceinline__ float es_sqrt(float v) { return sqrtf(v); }
-__device__ __forceinline__ double es_sqrt(double v) { return sqrt(v); }
 __device__ __forceinline__ float es_ceil(float v) { return ceilf(v); }
 __device__ __forceinline__ double es_ceil(double v) { return ceil(v); }
+
+// ES kernel value phi_beta(z) = exp(beta (sqrt(1 - z^2) - 1)), eq. (5).
+// float: hardware approximate square root and base-2 exponential, with
+// beta_e = beta * log2(e) folded in; double: the accurate library functions
+// with beta_e = beta.  1 - z^2 is formed with one fused multiply-add and
+// clamped at 0, so rounding just outside [-1, 1] gives phi = e^-beta.
+__device__ __forceinline__ float es_fast(float z, float beta_e) {
+  float q = fmaxf(fmaf(-z, z, 1.0f), 0.0f);
+  float s, r;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(s) : "f"(q));
+  const float arg = fmaf(beta_e, s, -beta_e);
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(arg));
+  return r;
+}
+__device__ __forceinline__ double es_fast(double z, double beta_e) {
+  double q = fma(-z, z, 1.0);
+  q = q > 0.0 ? q : 0.0;
+  return exp(beta_e * (sqrt(q) - 1.0));
+}
+
+// beta in the form es_fast takes for precision T.
+inline double es_beta_e(double beta, size_t real_bytes) {
+  return real_bytes == 4 ? beta * 1.4426950408889634 : beta;
+}
 
 // Kernel values of one point in one dimension: k[t] = phi_beta(z_t) for the
 // w nodes l0 + t.  Returns l0 (relative to the bin origin).
 template <typename T, int W>
-__device__ __forceinline__ int es_weights(T g, T beta, T (&k)[W]) {
+__device__ __forceinline__ int es_weights(T g, T beta_e, T (&k)[W]) {
   const T l0 = es_ceil(g - T(0.5) * T(W));
   const T d = l0 - g;
   const T scale = T(2) / T(W);
 #pragma unroll
-  for (int t = 0; t < W; t++) {
-    const T z = (d + T(t)) * scale;
-    T q = (T(1) - z) * (T(1) + z);
-    q = q > T(0) ? q : T(0);
-    k[t] = es_exp(beta * (es_sqrt(q) - T(1)));
-  }
+  for (int t = 0; t < W; t++) k[t] = es_fast((d + T(t)) * scale, beta_e);
   return (int)l0;
+}
+
+// L2 cache policies.  Points are streamed once per transform (evict first);
+// the caller's strengths / results are gathered or scattered through the
+// permutation, 8 or 16 bytes per 32-byte sector, so they are kept in L2
+// (evict last) until the neighbouring points of the same sector are touched.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ float ld_hint(const float *a, uint64_t pol) {
+  float v;
+  asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ double ld_hint(const double *a, uint64_t pol) {
+  double v;
+  asm volatile("ld.global.nc.L2::cache_hint.f64 %0, [%1], %2;" : "=d"(v) : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ int32_t ld_hint(const int32_t *a, uint64_t pol) {
+  int32_t v;
+  asm volatile("ld.global.nc.L2::cache_hint.s32 %0, [%1], %2;" : "=r"(v) : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ float2 ld_hint(const float2 *a, uint64_t pol) {
+  float2 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;"
+               : "=f"(v.x), "=f"(v.y) : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ double2 ld_hint(const double2 *a, uint64_t pol) {
+  double2 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v2.f64 {%0, %1}, [%2], %3;"
+               : "=d"(v.x), "=d"(v.y) : "l"(a), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void st_hint(float2 *a, float2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;"
+               :: "l"(a), "f"(v.x), "f"(v.y), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(double2 *a, double2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.f64 [%0], {%1, %2}, %3;"
+               :: "l"(a), "d"(v.x), "d"(v.y), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ void grid_atomic_add(float2 *cell, float re, float im) {
@@ -84,7 +149,7 @@ struct SIParams {
   C *grid;
   const C *c_in;  // type 1 strengths (caller's order)
   C *c_out;       // type 2 results (caller's order)
-  T beta;
+  T beta;  // in the form es_fast takes (beta * log2(e) for float)
   int n1, n2, n3;
   int m1, m2, m3;
   int nb1, nb2;
@@ -206,28 +271,31 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
   int b1, b2, b3;
   bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
   const int p1 = a.m1 + 2 * PAD, p2 = a.m2 + 2 * PAD, p3 = DIM == 3 ? a.m3 + 2 * PAD : 1;
-  const int ncell = p1 * p2 * p3;
   const int o1 = b1 * a.m1 - PAD, o2 = b2 * a.m2 - PAD, o3 = DIM == 3 ? b3 * a.m3 - PAD : 0;
-  // stage the padded bin of the fine grid (periodic wrap) in shared memory
-  for (int i = threadIdx.x; i < ncell; i += blockDim.x) {
-    const int s1 = i % p1;
-    const int q = i / p1;
-    const int s2 = q % p2;
-    const int s3 = q / p2;
-    const int l1 = wrap_tile(o1 + s1, a.n1);
-    const int l2 = wrap_tile(o2 + s2, a.n2);
-    const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
-    tile[i] = a.grid[l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)];
+  // stage the padded bin of the fine grid (periodic wrap) in shared memory,
+  // one tile row per warp at a time, lanes along x
+  {
+    const int nwarps = blockDim.x >> 5, wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    for (int row = wid; row < p2 * p3; row += nwarps) {
+      const int s2 = row % p2, s3 = row / p2;
+      const int l2 = wrap_tile(o2 + s2, a.n2);
+      const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
+      const C *src = a.grid + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3);
+      C *dst = tile + row * p1;
+      for (int s1 = ln; s1 < p1; s1 += 32) dst[s1] = src[wrap_tile(o1 + s1, a.n1)];
+    }
   }
   __syncthreads();
 
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
   const int end = sp.start + sp.count;
   for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
     T k1[W], k2[W], k3[W];
-    const int s1 = es_weights<T, W>(a.g1[j], a.beta, k1) + PAD;
-    const int s2 = es_weights<T, W>(a.g2[j], a.beta, k2) + PAD;
+    const int s1 = es_weights<T, W>(ld_hint(a.g1 + j, pol_stream), a.beta, k1) + PAD;
+    const int s2 = es_weights<T, W>(ld_hint(a.g2 + j, pol_stream), a.beta, k2) + PAD;
     int s3 = 0;
-    if (DIM == 3) s3 = es_weights<T, W>(a.g3[j], a.beta, k3) + PAD;
+    if (DIM == 3) s3 = es_weights<T, W>(ld_hint(a.g3 + j, pol_stream), a.beta, k3) + PAD;
+    const int dst = ld_hint(a.perm + j, pol_stream);
     T ar = T(0), ai = T(0);
 #pragma unroll 1
     for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
@@ -252,7 +320,7 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
     C out;
     out.x = ar;
     out.y = ai;
-    a.c_out[a.perm[j]] = out;
+    st_hint(a.c_out + dst, out, pol_keep);
   }
 }
 
@@ -315,7 +383,7 @@ SIParams<T> make_params(const nufft_plan_s *p) {
   a.grid = static_cast<typename Cplx<T>::type *>(p->grid);
   a.c_in = nullptr;
   a.c_out = nullptr;
-  a.beta = (T)p->beta;
+  a.beta = (T)es_beta_e(p->beta, sizeof(T));
   a.n1 = (int)p->n[0];
   a.n2 = (int)p->n[1];
   a.n3 = (int)p->n[2];

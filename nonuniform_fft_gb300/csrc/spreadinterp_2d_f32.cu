@@ -4,4 +4,5 @@
 namespace nufft {
 template cudaError_t launch_spread_t<2, float>(const nufft_plan_s *, const void *);
 template cudaError_t launch_interp_t<2, float>(const nufft_plan_s *, void *);
+
 }  // namespace nufft

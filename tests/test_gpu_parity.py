@@ -125,9 +125,29 @@ for _dim, _N in ((2, (100, 70)), (3, (20, 24, 36))):
             T_CASES.append((_dim, _N, _dt, _eps))
 
 
-@pytest.mark.parametrize("method", [nf.METHOD_SM, nf.METHOD_GM_SORT])
+METHODS = [nf.METHOD_SM, nf.METHOD_GM_SORT, nf.METHOD_REGTILE]
+
+
+@pytest.mark.parametrize("cols", [1, 2, 4])
+@pytest.mark.parametrize("dt,eps", [("f32", 1e-2), ("f32", 1e-6), ("f64", 1e-9), ("f64", 1e-12)])
+def test_regtile_columns_per_lane(cols, dt, eps):
+    """The register-tile spreader with 1, 2 and 4 tile columns per lane, on a
+    grid whose width is not a multiple of the bin width (ragged last bin)."""
+    rng = np.random.default_rng(31)
+    N = (150, 90)
+    M = 30000
+    pts = _pts(2, M, "uniform", rng, dt)
+    c = _cplx(M, rng, dt)
+    opts = {"method": nf.METHOD_REGTILE, "regtile_cols": cols, "msub": 700}
+    f = gpu_transform(1, pts, c, N, eps, -1, dt, opts)
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, -1)) <= TOL_O2[dt]
+
+
+@pytest.mark.parametrize("method", METHODS)
 @pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
 def test_type1_matches_oracle(dim, N, dt, eps, method):
+    if method == nf.METHOD_REGTILE and dim == 3:
+        pytest.skip("register-tile spreading is 2D")
     rng = np.random.default_rng(21)
     M = 20000
     pts = _pts(dim, M, "uniform", rng, dt)
@@ -141,9 +161,11 @@ def test_type1_matches_oracle(dim, N, dt, eps, method):
         _check_direct(oracle.rel_l2(f, o1), oracle.rel_l2(o2, o1), eps)
 
 
-@pytest.mark.parametrize("method", [nf.METHOD_SM, nf.METHOD_GM_SORT])
+@pytest.mark.parametrize("method", METHODS)
 @pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
 def test_type2_matches_oracle(dim, N, dt, eps, method):
+    if method == nf.METHOD_REGTILE and dim == 3:
+        pytest.skip("register-tile spreading is 2D")
     rng = np.random.default_rng(22)
     M = 20000
     pts = _pts(dim, M, "uniform", rng, dt)
@@ -175,7 +197,8 @@ def test_adjoint_identity_on_gpu(dim, N, dt):
         assert abs(lhs - rhs) <= tol * abs(lhs)
 
 
-def test_clustered_points_single_bin():
+@pytest.mark.parametrize("method", METHODS)
+def test_clustered_points_single_bin(method):
     """Every point in one fine cell: one bin, many subproblems (SM step 1
     load balancing), heavy atomic contention."""
     rng = np.random.default_rng(9)
@@ -184,9 +207,10 @@ def test_clustered_points_single_bin():
     pts = [(0.3 + rng.uniform(0, h, M)).astype(np.float32) for _ in range(2)]
     c = _cplx(M, rng, "f32")
     info = {}
-    f = gpu_transform(1, pts, c, (128, 128), 1e-5, -1, "f32", plan_out=info)
-    assert info["nsub"] >= M // 1024
-    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, (128, 128), 1e-5, -1)) <= 1e-5
+    f = gpu_transform(1, pts, c, (128, 128), 1e-5, -1, "f32", {"method": method}, plan_out=info)
+    assert info["nsub"] >= M // 2048
+    ref = oracle.nufft_type1(pts, c, (128, 128), 1e-5, -1)
+    assert oracle.rel_l2(f, ref) <= 1e-5
 
 
 @pytest.mark.parametrize("N", [(1, 1), (2, 3), (1, 4, 2)])
@@ -259,11 +283,18 @@ def test_errors_reported():
         assert ei.value.code == nf.ERR_BAD_OPT
         # too-large bins for shared memory are refused at setpts
         big = [torch.zeros(4, device=DEV), torch.zeros(4, device=DEV)]
-        p2 = nf.Plan(1, (2048, 2048), -1, 1e-5, "complex64", bin1=1024, bin2=1024)
+        p2 = nf.Plan(1, (2048, 2048), -1, 1e-5, "complex64", bin1=1024, bin2=1024,
+                     method=nf.METHOD_SM)
         with pytest.raises(nf.NufftError) as ei:
             p2.setpts(*big)
         assert ei.value.code == nf.ERR_BAD_OPT
         p2.close()
+        # the register-tile method is 2D only
+        p3 = nf.Plan(1, (16, 16, 16), -1, 1e-5, "complex64", method=nf.METHOD_REGTILE)
+        with pytest.raises(nf.NufftError) as ei:
+            p3.setpts(*[torch.zeros(4, device=DEV)] * 3)
+        assert ei.value.code == nf.ERR_BAD_OPT
+        p3.close()
     finally:
         plan.close()
 
