@@ -90,7 +90,7 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_METHOD_AUTO 0
 #define NUFFT_METHOD_SM 1          /* Sec. III-A "SM": subproblems spread in shared memory */
 #define NUFFT_METHOD_GM_SORT 2     /* Sec. III-A "GM-sort": thread per sorted point, global atomics */
-#define NUFFT_METHOD_REGTILE 3     /* SM decomposition with the padded bin in registers (2D type 1) */
+#define NUFFT_METHOD_REGTILE 3     /* SM decomposition with the padded bin in registers (type 1) */
 
 /*
  * Create a plan.  Defined by Sec. I-A ("plan, setup, execute, destroy") and
@@ -116,9 +116,10 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
  * Set a tuning option; takes effect at the next setpts.  Keys:
  *   "method"   NUFFT_METHOD_* (type 1 spreading; type 2 always uses the
  *              tiled shared-memory interpolator unless "method" is GM_SORT).
- *              AUTO picks REGTILE for 2D type 1 and SM otherwise.  REGTILE
- *              fixes the bin size (the "bin" options are ignored), is 2D only,
- *              and type 2 plans with it interpolate with the SM kernel.
+ *              AUTO picks REGTILE for type 1 and SM for type 2.  REGTILE
+ *              fixes the bin size (the "bin" options are ignored, except
+ *              "bin2" in 3D), and type 2 plans with it interpolate with the SM
+ *              kernel.
  *   "bin1", "bin2", "bin3"   bin size m_i in fine-grid cells (Sec. III-A), >= 1.
  *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1.
  *   "threads"  threads per block of the SM / GM-sort spreading and

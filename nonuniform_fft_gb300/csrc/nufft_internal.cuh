@@ -117,6 +117,11 @@ cudaError_t launch_interp_t(const nufft_plan_s *p, void *c);
 template <typename T>
 cudaError_t launch_spread_regtile2d(const nufft_plan_s *p, const void *c);
 void regtile2d_bins(int w, int cols, int *m1, int *m2);
+// Register-tile 3D spreader (spread_plane3d.cuh), instantiated in
+// spread_plane3d_{f32,f64}.cu, and the bin size it is built for.
+template <typename T>
+cudaError_t launch_spread_plane3d(const nufft_plan_s *p, const void *c);
+void plane3d_bins(int w, int dtype, int *m1, int *m2, int *m3);
 
 // deconv.cu: type 1 correction + truncation, type 2 correction + padding.
 cudaError_t launch_deconvolve(const nufft_plan_s *p, void *f);

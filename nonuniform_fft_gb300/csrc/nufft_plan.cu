@@ -335,14 +335,20 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   // resolve options
   p->method = p->opt_method;
   if (p->method == NUFFT_METHOD_AUTO)
-    p->method = p->dim == 2 && p->type == 1 ? NUFFT_METHOD_REGTILE : NUFFT_METHOD_SM;
-  if (p->method == NUFFT_METHOD_REGTILE && p->dim != 2) return NUFFT_ERR_BAD_OPT;
+    p->method = p->type == 1 ? NUFFT_METHOD_REGTILE : NUFFT_METHOD_SM;
   int m[3];
   default_bins(p, m);
   for (int d = 0; d < 3; d++)
     if (d < p->dim && p->opt_bin[d] > 0) m[d] = p->opt_bin[d];
   p->regtile_cols = p->opt_regtile_cols > 0 ? p->opt_regtile_cols : 1;
-  if (p->method == NUFFT_METHOD_REGTILE) nufft::regtile2d_bins(p->w, p->regtile_cols, &m[0], &m[1]);
+  if (p->method == NUFFT_METHOD_REGTILE) {
+    if (p->dim == 2) {
+      nufft::regtile2d_bins(p->w, p->regtile_cols, &m[0], &m[1]);
+    } else {
+      nufft::plane3d_bins(p->w, p->dtype, &m[0], &m[1], &m[2]);
+      if (p->opt_bin[1] > 0) m[1] = p->opt_bin[1];  // rows are free
+    }
+  }
   for (int d = 0; d < 3; d++) {
     if (d >= p->dim) m[d] = 1;
     if (m[d] > p->n[d]) m[d] = (int)p->n[d];
@@ -358,7 +364,8 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
     p->nbins *= p->nb[d];
   }
   p->msub = p->opt_msub > 0 ? p->opt_msub
-                            : (p->method == NUFFT_METHOD_REGTILE ? 512 : (p->type == 2 ? 2048 : 1024));
+                            : (p->method == NUFFT_METHOD_REGTILE ? (p->dim == 2 ? 512 : 8192)
+                                                                 : (p->type == 2 ? 2048 : 1024));
   // the cell-level sort indexes (bin, cell) pairs with int32
   if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
   p->threads = p->opt_threads > 0 ? p->opt_threads : 256;
@@ -434,9 +441,12 @@ int nufft_execute(nufft_plan_t p, void *c, void *f) {
   };
   auto spread = [&]() -> cudaError_t {
     if (p->nsub == 0) return cudaSuccess;
-    if (p->method == NUFFT_METHOD_REGTILE)
+    if (p->method == NUFFT_METHOD_REGTILE && p->dim == 2)
       return p->dtype == 0 ? nufft::launch_spread_regtile2d<float>(p, dc)
                            : nufft::launch_spread_regtile2d<double>(p, dc);
+    if (p->method == NUFFT_METHOD_REGTILE)
+      return p->dtype == 0 ? nufft::launch_spread_plane3d<float>(p, dc)
+                           : nufft::launch_spread_plane3d<double>(p, dc);
     if (p->dim == 2)
       return p->dtype == 0 ? nufft::launch_spread_t<2, float>(p, dc) : nufft::launch_spread_t<2, double>(p, dc);
     return p->dtype == 0 ? nufft::launch_spread_t<3, float>(p, dc) : nufft::launch_spread_t<3, double>(p, dc);

@@ -146,8 +146,6 @@ def test_regtile_columns_per_lane(cols, dt, eps):
 @pytest.mark.parametrize("method", METHODS)
 @pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
 def test_type1_matches_oracle(dim, N, dt, eps, method):
-    if method == nf.METHOD_REGTILE and dim == 3:
-        pytest.skip("register-tile spreading is 2D")
     rng = np.random.default_rng(21)
     M = 20000
     pts = _pts(dim, M, "uniform", rng, dt)
@@ -211,6 +209,23 @@ def test_clustered_points_single_bin(method):
     assert info["nsub"] >= M // 2048
     ref = oracle.nufft_type1(pts, c, (128, 128), 1e-5, -1)
     assert oracle.rel_l2(f, ref) <= 1e-5
+
+
+@pytest.mark.parametrize("dt,eps", [("f32", 1e-6), ("f64", 1e-12), ("f64", 1e-3)])
+@pytest.mark.parametrize("msub", [100000, 500])
+def test_regtile3d_clustered_and_ragged(dt, eps, msub):
+    """3D register-tile spreading on a grid that is not a multiple of the bin
+    (ragged last bins in every dimension), with a cluster that puts many
+    subproblems in a few bins."""
+    rng = np.random.default_rng(41)
+    N = (30, 22, 26)
+    M = 40000
+    pts = _pts(3, M, "uniform", rng, dt)
+    for a in pts:
+        a[: M // 2] = (np.mod(rng.normal(0.5, 0.08, M // 2) + np.pi, 2 * np.pi) - np.pi).astype(a.dtype)
+    c = _cplx(M, rng, dt)
+    f = gpu_transform(1, pts, c, N, eps, 1, dt, {"method": nf.METHOD_REGTILE, "msub": msub})
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, 1)) <= TOL_O2[dt]
 
 
 @pytest.mark.parametrize("N", [(1, 1), (2, 3), (1, 4, 2)])
@@ -289,12 +304,7 @@ def test_errors_reported():
             p2.setpts(*big)
         assert ei.value.code == nf.ERR_BAD_OPT
         p2.close()
-        # the register-tile method is 2D only
-        p3 = nf.Plan(1, (16, 16, 16), -1, 1e-5, "complex64", method=nf.METHOD_REGTILE)
-        with pytest.raises(nf.NufftError) as ei:
-            p3.setpts(*[torch.zeros(4, device=DEV)] * 3)
-        assert ei.value.code == nf.ERR_BAD_OPT
-        p3.close()
+
     finally:
         plan.close()
 
