@@ -1,11 +1,12 @@
 #!/usr/bin/env python3
 """Throughput benchmark of the nonuniform FFT hot path on GB300.
 
-One step = one type 1 transform (spread -> FFT -> correct) plus one type 2
-transform (correct/pad -> FFT -> interpolate) of the workload's M points,
-each through the C ABI, with the points already bin-sorted (setpts is
-excluded, as in the metric).  value = nonuniform points transformed per
-second over the whole job: 2 M per step per GPU (type 1 + type 2).
+One step = one type 1 transform (spread -> FFT -> correct) plus, for
+workloads that have one, one type 2 transform (correct/pad -> FFT ->
+interpolate) of the workload's M points, each through the C ABI, with the
+points already bin-sorted (setpts is excluded, as in the metric).  value =
+nonuniform points transformed per second over the whole job: M per transform
+per step per GPU.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle (the
 three-step NUFFT in double precision, single thread) on a bounded sample of
@@ -164,9 +165,19 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
+def cpu_sample_points(wl: W.Workload, budget_cells: float = 1.2e8) -> int:
+    """Points in a CPU-oracle sample: about budget_cells kernel-weighted grid
+    updates per transform (w^d per point), so that every workload's sample
+    takes seconds, not minutes."""
+    import oracle
+    w = oracle.es_params(wl.eps)[0]
+    return int(min(wl.M, max(20000, budget_cells / w ** wl.dim)))
+
+
 def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1) -> dict:
-    """Time the oracle's three-step NUFFT (type 1 + type 2) on the first
-    sample_M points of the workload; returns points/s over `steps` repeats."""
+    """Time the oracle's three-step NUFFT (type 1, plus type 2 when the
+    workload has it) on the first sample_M points of the workload; returns
+    points/s over `steps` repeats."""
     import oracle
     sub = wl.scaled(M=sample_M)
     pts, c = W.sample(sub)
@@ -175,12 +186,15 @@ def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1) -> dict:
     t0 = time.perf_counter()
     for _ in range(steps):
         oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1])
-        oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2])
+        if 2 in wl.types:
+            oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2])
     dt = time.perf_counter() - t0
-    return {"value": 2 * sample_M * steps / dt, "unit": "NU points/s", "cores": 1,
+    per_step = sample_M * len(wl.types)
+    types = " + ".join(f"type {t}" for t in wl.types)
+    return {"value": per_step * steps / dt, "unit": "NU points/s", "cores": 1,
             "kind": "oracle", "seconds": dt,
             "sample": f"{sample_M} of {wl.M} points of {wl.name}, full {'x'.join(map(str, wl.N))} "
-                      f"modes, type 1 + type 2, x{steps}; double precision, one thread"}
+                      f"modes, {types}, x{steps}; double precision, one thread"}
 
 
 def run_reference(args, wl):
@@ -188,7 +202,8 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     # bounded: about a minute of CPU work for the whole --steps + --warmup run
-    per_step = args.cpu_sample or max(20000, int(1.5e6 / max(1, args.steps + args.warmup)))
+    per_step = args.cpu_sample or max(
+        5000, cpu_sample_points(wl, 1.2e8 / max(1, (args.steps + args.warmup) / 2)))
     per_step = min(per_step, wl.M)
     if args.warmup:
         cpu_oracle_run(wl, min(per_step, 20000), 1)
@@ -240,15 +255,20 @@ def run_ours(args, wl):
     del pts
 
     p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream)
-    p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream)
     p1.setpts(*xs)
-    p2.setpts(*xs)
+    p2 = None
+    if 2 in wl.types:
+        p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream)
+        p2.setpts(*xs)
     info = p1.info()
     n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
 
+    has2 = 2 in wl.types
+
     def step():
         p1.execute(c_in, f_out)
-        p2.execute(c_out, f_in)
+        if has2:
+            p2.execute(c_out, f_in)
 
     for _ in range(args.warmup):
         step()
@@ -268,7 +288,7 @@ def run_ours(args, wl):
             step()
             ev1[i].record(stream)
             t1 = p1.timings()                       # waits for this step's events
-            t2 = p2.timings()
+            t2 = p2.timings() if has2 else {k: 0.0 for k in nf.TIMING_KEYS}
             stage["spread"] += t1["spread_interp"]
             stage["fft1"] += t1["fft"]
             stage["deconv"] += t1["deconv_pad"]
@@ -281,24 +301,32 @@ def run_ours(args, wl):
         dist.barrier()
     total_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1))
     t_max = reduce_max(total_ms, dev)
-    pts_per_step = 2 * wl.M
+    pts_per_step = wl.M * len(wl.types)
     value = job_throughput(world, pts_per_step, args.steps, t_max / 1e3)
 
     # roofline of the dominant kernel (per-launch averages over the timed region)
     K = args.steps
     algo = algorithmic_bytes(wl, n)
-    per_launch = {"spread": stage["spread"] / K, "interp": stage["interp"] / K}
+    per_launch = {"spread": stage["spread"] / K}
+    if has2:
+        per_launch["interp"] = stage["interp"] / K
     dom = max(per_launch, key=per_launch.get)
-    with open(PEAKS_PATH) as fh:
-        peaks = json.load(fh)
-    peak = float(peaks["hbm_gbs"])
+    try:
+        with open(PEAKS_PATH) as fh:
+            peak = float(json.load(fh)["hbm_gbs"])
+        peak_source = "MEASURED_PEAKS.json hbm_gbs (measured copy bandwidth)"
+    except (OSError, ValueError, KeyError):
+        peak, peak_source = 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
     achieved = algo[dom] / (per_launch[dom] / 1e3) / 1e9
-    kernel_name = {"spread": "spread_sm_kernel", "interp": "interp_sm_kernel"}[dom]
+    spread_kernel = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
+                     nf.METHOD_REGTILE: "spread_regtile2d_kernel" if wl.dim == 2
+                     else "spread_plane3d_kernel"}[info["method"]]
+    kernel_name = {"spread": spread_kernel, "interp": "interp_sm_kernel"}[dom]
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,
                 "traffic": load_traffic(kernel_name, wl.name),
                 "algorithmic_bytes_per_launch": algo[dom], "launch_ms": per_launch[dom],
-                "peak_source": "MEASURED_PEAKS.json hbm_gbs (measured copy bandwidth)"}
+                "peak_source": peak_source}
 
     # end to end through the C ABI with pinned host buffers
     e2e = None
@@ -308,24 +336,26 @@ def run_ours(args, wl):
         hf_out = torch.empty(int(np.prod(N)), dtype=ctorch).pin_memory()
         hc_out = torch.empty(wl.M, dtype=ctorch).pin_memory()
         p1.execute(hc, hf_out)
-        p2.execute(hc_out, hf)
+        if has2:
+            p2.execute(hc_out, hf)
         e2e_steps = max(3, min(args.steps, 10))
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             p1.execute(hc, hf_out)        # host c in, host f out (synchronous)
-            p2.execute(hc_out, hf)        # host f in, host c out (synchronous)
+            if has2:
+                p2.execute(hc_out, hf)    # host f in, host c out (synchronous)
         el = reduce_max(time.perf_counter() - t0, dev)
         cb = hc.element_size()
         modes = int(np.prod(N))
         e2e = {"value": job_throughput(world, pts_per_step, e2e_steps, el), "unit": "NU points/s",
-               "h2d_bytes_per_step": wl.M * cb + modes * cb,
-               "d2h_bytes_per_step": modes * cb + wl.M * cb}
+               "h2d_bytes_per_step": wl.M * cb + (modes * cb if has2 else 0),
+               "d2h_bytes_per_step": modes * cb + (wl.M * cb if has2 else 0)}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_run(wl, args.cpu_sample or min(wl.M, 3_000_000), 1)
+        cpu = cpu_oracle_run(wl, args.cpu_sample or cpu_sample_points(wl), 1)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:
@@ -337,7 +367,8 @@ def run_ours(args, wl):
             "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": wl.name, "dim": wl.dim, "N": list(wl.N), "M": wl.M,
                        "eps": wl.eps, "w": info["w"], "fine_grid": n, "dist": wl.dist,
-                       "types": "type 1 (iflag -1) + type 2 (iflag +1) per step",
+                       "types": " + ".join(f"type {t} (iflag {wl.iflag[t]:+d})" for t in wl.types)
+                                + " per step",
                        "points_per_step_per_gpu": pts_per_step,
                        "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
                        "msub": info["msub"], "nsub": info["nsub"],
@@ -348,12 +379,13 @@ def run_ours(args, wl):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 4 * K,
+            "gpu_launches": (4 if has2 else 2) * K,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     p1.close()
-    p2.close()
+    if p2 is not None:
+        p2.close()
     if world > 1:
         dist.destroy_process_group()
     return 0

@@ -7,6 +7,7 @@
 // correction factors of eq. (10)), the fine grid, the cuFFT plan used for
 // eq. (9) / (12), and the bin-sort results of Sec. III-A that setpts
 // produces; execute runs the three steps on the plan's stream.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -363,9 +364,17 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
     p->nb[d] = (int)((p->n[d] + m[d] - 1) / m[d]);
     p->nbins *= p->nb[d];
   }
-  p->msub = p->opt_msub > 0 ? p->opt_msub
-                            : (p->method == NUFFT_METHOD_REGTILE ? (p->dim == 2 ? 512 : 8192)
-                                                                 : (p->type == 2 ? 2048 : 1024));
+  if (p->opt_msub > 0) {
+    p->msub = p->opt_msub;
+  } else if (p->method == NUFFT_METHOD_REGTILE) {
+    // a subproblem is one warp (2D) or one block (3D) walking rows in order:
+    // cap it so that small problems still spread over every SM
+    const int64_t cap = p->dim == 2 ? 512 : 8192;
+    const int64_t fill = M / (p->dim == 2 ? 152 * 32 : 152 * 4);
+    p->msub = (int)std::max<int64_t>(64, std::min<int64_t>(cap, fill));
+  } else {
+    p->msub = p->type == 2 ? 2048 : 1024;
+  }
   // the cell-level sort indexes (bin, cell) pairs with int32
   if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
   p->threads = p->opt_threads > 0 ? p->opt_threads : 256;

@@ -289,13 +289,32 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
 
   const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
   const int end = sp.start + sp.count;
-  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+  // software pipeline: the next point's coordinates and destination are
+  // loaded before the current point is computed
+  int j = sp.start + threadIdx.x;
+  T nx = T(0), ny = T(0), nz = T(0);
+  int ndst = 0;
+  if (j < end) {
+    nx = ld_hint(a.g1 + j, pol_stream);
+    ny = ld_hint(a.g2 + j, pol_stream);
+    if (DIM == 3) nz = ld_hint(a.g3 + j, pol_stream);
+    ndst = ld_hint(a.perm + j, pol_stream);
+  }
+  for (; j < end; j += blockDim.x) {
+    const T gx = nx, gy = ny, gz = nz;
+    const int dst = ndst;
+    const int jn = j + blockDim.x;
+    if (jn < end) {
+      nx = ld_hint(a.g1 + jn, pol_stream);
+      ny = ld_hint(a.g2 + jn, pol_stream);
+      if (DIM == 3) nz = ld_hint(a.g3 + jn, pol_stream);
+      ndst = ld_hint(a.perm + jn, pol_stream);
+    }
     T k1[W], k2[W], k3[W];
-    const int s1 = es_weights<T, W>(ld_hint(a.g1 + j, pol_stream), a.beta, k1) + PAD;
-    const int s2 = es_weights<T, W>(ld_hint(a.g2 + j, pol_stream), a.beta, k2) + PAD;
+    const int s1 = es_weights<T, W>(gx, a.beta, k1) + PAD;
+    const int s2 = es_weights<T, W>(gy, a.beta, k2) + PAD;
     int s3 = 0;
-    if (DIM == 3) s3 = es_weights<T, W>(ld_hint(a.g3 + j, pol_stream), a.beta, k3) + PAD;
-    const int dst = ld_hint(a.perm + j, pol_stream);
+    if (DIM == 3) s3 = es_weights<T, W>(gz, a.beta, k3) + PAD;
     T ar = T(0), ai = T(0);
 #pragma unroll 1
     for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
