@@ -51,7 +51,17 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="points per transform in the CPU baseline sample (0: auto)")
+    ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
+                    help="plan option for both plans (nufft_set_opt), e.g. msub=1024; repeatable")
     return ap.parse_args()
+
+
+def plan_opts(args) -> dict:
+    out = {}
+    for kv in args.opt:
+        k, v = kv.split("=", 1)
+        out[k] = float(v)
+    return out
 
 
 # ------------------------------------------------------------------ helpers
@@ -254,11 +264,12 @@ def run_ours(args, wl):
     stream.synchronize()
     del pts
 
-    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream)
+    opts = plan_opts(args)
+    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream, **opts)
     p1.setpts(*xs)
     p2 = None
     if 2 in wl.types:
-        p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream)
+        p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream, **opts)
         p2.setpts(*xs)
     info = p1.info()
     n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
@@ -373,6 +384,7 @@ def run_ours(args, wl):
                        "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
                        "msub": info["msub"], "nsub": info["nsub"],
                        "l2": "flushed between timed steps (256 MiB write, untimed)",
+                       "plan_options": opts,
                        "parallelism": f"replicas x{world}"},
             "stage_ms_per_step": {k: v / K for k, v in stage.items()},
             "step_ms_rank0": steps_ms,
