@@ -330,9 +330,12 @@ def run_ours(args, wl):
         peak, peak_source = 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
     achieved = algo[dom] / (per_launch[dom] / 1e3) / 1e9
     spread_kernel = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
+                     nf.METHOD_GM: "spread_gmu_kernel",
                      nf.METHOD_REGTILE: "spread_regtile2d_kernel" if wl.dim == 2
                      else "spread_plane3d_kernel"}[info["method"]]
-    kernel_name = {"spread": spread_kernel, "interp": "interp_sm_kernel"}[dom]
+    interp_kernel = {nf.METHOD_GM_SORT: "interp_gm_kernel", nf.METHOD_GM: "interp_gmu_kernel"}.get(
+        p2.info()["method"] if has2 else 0, "interp_sm_kernel")
+    kernel_name = {"spread": spread_kernel, "interp": interp_kernel}[dom]
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,
                 "traffic": load_traffic(kernel_name, wl.name),
@@ -364,6 +367,23 @@ def run_ours(args, wl):
                "h2d_bytes_per_step": wl.M * cb + (modes * cb if has2 else 0),
                "d2h_bytes_per_step": modes * cb + (wl.M * cb if has2 else 0)}
 
+    # timing scopes of [cuFINUFFT] Sec. IV-C: "exec" (the step above), "total"
+    # (setpts + exec, on the device) and "total+mem" (host arrays in and out,
+    # setpts and exec, wall clock, synchronous)
+    setpts_ms = p1.timings()["setpts"] + (p2.timings()["setpts"] if has2 else 0.0)
+    scopes = {"exec_ms": t_max / K, "setpts_ms": setpts_ms, "total_ms": t_max / K + setpts_ms}
+    if not args.no_e2e:
+        hx = [x.cpu().pin_memory() for x in xs]
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        p1.setpts(*hx)
+        p1.execute(hc, hf_out)
+        if has2:
+            p2.setpts(*hx)
+            p2.execute(hc_out, hf)
+        torch.cuda.synchronize()
+        scopes["total_mem_ms"] = 1e3 * (time.perf_counter() - t0)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_oracle_run(wl, args.cpu_sample or cpu_sample_points(wl), 1)
@@ -387,6 +407,7 @@ def run_ours(args, wl):
                        "plan_options": opts,
                        "parallelism": f"replicas x{world}"},
             "stage_ms_per_step": {k: v / K for k, v in stage.items()},
+            "scopes": scopes,
             "step_ms_rank0": steps_ms,
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -91,6 +91,7 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_METHOD_SM 1          /* Sec. III-A "SM": subproblems spread in shared memory */
 #define NUFFT_METHOD_GM_SORT 2     /* Sec. III-A "GM-sort": thread per sorted point, global atomics */
 #define NUFFT_METHOD_REGTILE 3     /* SM decomposition with the padded bin in registers (type 1) */
+#define NUFFT_METHOD_GM 4          /* Sec. III-A/B "GM": thread per point in the caller's order, no sort */
 
 /*
  * Create a plan.  Defined by Sec. I-A ("plan, setup, execute, destroy") and
@@ -177,7 +178,8 @@ int nufft_get_info(nufft_plan_t plan, int64_t *info, int n);
  *                     (points of bin 0, then bin 1, ...; order inside a bin is
  *                     unspecified);
  *   subprob[3*nsub]   (bin, first sorted slot, point count) per subproblem.
- * Synchronises the plan's stream.  Errors: BAD_ARG, NO_POINTS, CUDA.
+ * Synchronises the plan's stream.  Errors: BAD_ARG, NO_POINTS, BAD_OPT (the
+ * GM method sorts nothing), CUDA.
  */
 int nufft_get_sort(nufft_plan_t plan, int32_t *counts, int32_t *starts, int32_t *perm,
                    int32_t *subprob);

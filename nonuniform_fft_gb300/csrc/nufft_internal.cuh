@@ -103,6 +103,8 @@ inline int64_t mode_count(const nufft_plan_s *p) { return p->N[0] * p->N[1] * p-
 
 // setpts.cu: bin sort and subproblem table.  Returns a NUFFT_* code.
 int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z);
+// setpts.cu: GM (unsorted) method: per-point cells and offsets only.
+int run_setpts_gm(nufft_plan_s *p, const void *x, const void *y, const void *z);
 
 // spreadinterp_*.cu: type 1 spreading (grid must be zeroed) and type 2
 // interpolation, for the plan's dim, dtype and width.

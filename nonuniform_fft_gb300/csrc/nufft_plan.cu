@@ -306,7 +306,7 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
   const int64_t v = (int64_t)value;
   if (!std::strcmp(key, "method")) {
     if (v != NUFFT_METHOD_AUTO && v != NUFFT_METHOD_SM && v != NUFFT_METHOD_GM_SORT &&
-        v != NUFFT_METHOD_REGTILE)
+        v != NUFFT_METHOD_REGTILE && v != NUFFT_METHOD_GM)
       return NUFFT_ERR_BAD_OPT;
     p->opt_method = (int)v;
   } else if (!std::strcmp(key, "bin1") || !std::strcmp(key, "bin2") || !std::strcmp(key, "bin3")) {
@@ -375,6 +375,8 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   } else {
     p->msub = p->type == 2 ? 2048 : 1024;
   }
+  // GM packs a point's cell index into int32
+  if (p->method == NUFFT_METHOD_GM && nufft::grid_cells(p) >= (int64_t(1) << 31)) return NUFFT_ERR_TOO_LARGE;
   // the cell-level sort indexes (bin, cell) pairs with int32
   if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
   p->threads = p->opt_threads > 0 ? p->opt_threads : 256;
@@ -399,7 +401,8 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
     }
   }
   if (cudaEventRecord(p->ev[EV_SET0], p->stream) != cudaSuccess) return NUFFT_ERR_CUDA;
-  const int rc = nufft::run_setpts(p, xyz[0], xyz[1], xyz[2]);
+  const int rc = p->method == NUFFT_METHOD_GM ? nufft::run_setpts_gm(p, xyz[0], xyz[1], xyz[2])
+                                              : nufft::run_setpts(p, xyz[0], xyz[1], xyz[2]);
   if (rc) {
     cudaGetLastError();
     return rc;
@@ -449,7 +452,7 @@ int nufft_execute(nufft_plan_t p, void *c, void *f) {
     return r == CUFFT_SUCCESS ? NUFFT_OK : NUFFT_ERR_CUFFT;
   };
   auto spread = [&]() -> cudaError_t {
-    if (p->nsub == 0) return cudaSuccess;
+    if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
     if (p->method == NUFFT_METHOD_REGTILE && p->dim == 2)
       return p->dtype == 0 ? nufft::launch_spread_regtile2d<float>(p, dc)
                            : nufft::launch_spread_regtile2d<double>(p, dc);
@@ -461,7 +464,7 @@ int nufft_execute(nufft_plan_t p, void *c, void *f) {
     return p->dtype == 0 ? nufft::launch_spread_t<3, float>(p, dc) : nufft::launch_spread_t<3, double>(p, dc);
   };
   auto interp = [&]() -> cudaError_t {
-    if (p->nsub == 0) return cudaSuccess;
+    if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
     if (p->dim == 2)
       return p->dtype == 0 ? nufft::launch_interp_t<2, float>(p, dc) : nufft::launch_interp_t<2, double>(p, dc);
     return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);
@@ -554,6 +557,7 @@ int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
 int nufft_get_sort(nufft_plan_t p, int32_t *counts, int32_t *starts, int32_t *perm, int32_t *subprob) {
   if (!p) return NUFFT_ERR_BAD_ARG;
   if (!p->have_pts) return NUFFT_ERR_NO_POINTS;
+  if (p->method == NUFFT_METHOD_GM) return NUFFT_ERR_BAD_OPT;
   if (cudaSetDevice(p->device) != cudaSuccess || cudaStreamSynchronize(p->stream) != cudaSuccess)
     return NUFFT_ERR_CUDA;
   const size_t nb = (size_t)p->nbins * 4;

@@ -150,6 +150,29 @@ __global__ void bins_from_cells_kernel(const int32_t *cell_starts, int64_t nbins
   if (b < nbins) counts[b] = cell_starts[(b + 1) * cpb] - s0;
 }
 
+// GM (no sort): each point's fine-grid cell, packed l1 + n1 (l2 + n2 l3), and
+// its offset inside the cell, in the caller's order.
+template <typename T>
+__global__ void gm_prepare_kernel(PointsIn a, int32_t *packed, T *f0, T *f1, T *f2, int *flag) {
+  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= a.M) return;
+  T *out[3] = {f0, f1, f2};
+  bool bad = false;
+  int64_t cell_index = 0, stride = 1;
+  for (int d = 0; d < a.dim; d++) {
+    double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
+    int cell = (int)floor(g);
+    if (cell >= a.n[d]) cell = a.n[d] - 1;
+    T v = (T)(g - (double)cell);  // exact in double, then rounded to T
+    if (v >= T(1)) v = below(T(1));
+    out[d][j] = v;
+    cell_index += (int64_t)cell * stride;
+    stride *= a.n[d];
+  }
+  if (bad) atomicOr(flag, 1);
+  packed[j] = (int32_t)cell_index;
+}
+
 __global__ void sub_count_kernel(const int32_t *counts, int64_t nbins, int msub, int32_t *nsub) {
   const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= nbins) return;
@@ -316,6 +339,66 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
         p->bin_counts, p->bin_starts, p->sub_starts, p->nbins, p->nsub, p->msub, p->subprob);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
+  return NUFFT_OK;
+}
+
+// GM setpts: no bin sort, only the per-point cell and offset.
+int run_setpts_gm(nufft_plan_s *p, const void *x, const void *y, const void *z) {
+  const int64_t M = p->M;
+  cudaStream_t s = p->stream;
+  const size_t rs = real_size(p);
+  if (M > p->cap_pts || !p->perm) {
+    cudaFree(p->perm);
+    cudaFree(p->bin_of);
+    cudaFree(p->rank_of);
+    for (int d = 0; d < 3; d++) cudaFree(p->gcoord[d]);
+    p->perm = p->bin_of = p->rank_of = nullptr;
+    p->gcoord[0] = p->gcoord[1] = p->gcoord[2] = nullptr;
+    p->cap_pts = 0;
+    const size_t mm = (size_t)(M > 0 ? M : 1);
+    if (cudaMalloc((void **)&p->perm, mm * 4) != cudaSuccess ||
+        cudaMalloc((void **)&p->bin_of, mm * 4) != cudaSuccess ||
+        cudaMalloc((void **)&p->rank_of, mm * 4) != cudaSuccess)
+      return NUFFT_ERR_ALLOC;
+    for (int d = 0; d < p->dim; d++)
+      if (cudaMalloc(&p->gcoord[d], mm * rs) != cudaSuccess) return NUFFT_ERR_ALLOC;
+    p->cap_pts = M;
+  }
+  if (!p->flag && cudaMalloc((void **)&p->flag, sizeof(int)) != cudaSuccess) return NUFFT_ERR_ALLOC;
+  PointsIn a;
+  a.x[0] = x;
+  a.x[1] = y;
+  a.x[2] = p->dim == 3 ? z : x;
+  a.M = M;
+  a.dim = p->dim;
+  a.is_double = p->dtype;
+  a.inv_two_pi = 1.0 / (2.0 * 3.14159265358979323846);
+  for (int d = 0; d < 3; d++) {
+    a.n[d] = (int)p->n[d];
+    a.m[d] = p->m[d];
+    a.nb[d] = p->nb[d];
+  }
+  if (cudaMemsetAsync(p->flag, 0, sizeof(int), s) != cudaSuccess) return NUFFT_ERR_CUDA;
+  const int threads = 256;
+  if (M > 0) {
+    const unsigned blocks = (unsigned)((M + threads - 1) / threads);
+    if (p->dtype == 0)
+      gm_prepare_kernel<float><<<blocks, threads, 0, s>>>(
+          a, p->bin_of, (float *)p->gcoord[0], (float *)p->gcoord[1],
+          (float *)(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]), p->flag);
+    else
+      gm_prepare_kernel<double><<<blocks, threads, 0, s>>>(
+          a, p->bin_of, (double *)p->gcoord[0], (double *)p->gcoord[1],
+          (double *)(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]), p->flag);
+    if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+  int host_flag = 0;
+  if (cudaMemcpyAsync(&host_flag, p->flag, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return NUFFT_ERR_CUDA;
+  if (host_flag) return NUFFT_ERR_BAD_POINTS;
+  p->nsub = 0;
+  p->nbins = 0;
   return NUFFT_OK;
 }
 

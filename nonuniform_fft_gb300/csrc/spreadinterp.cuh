@@ -389,6 +389,100 @@ __global__ void interp_gm_kernel(SIParams<T> a) {
   }
 }
 
+// ---------------------------------------------------------------- GM (unsorted)
+// [cuFINUFFT] Sec. III-A "GM": one thread per point in the caller's order,
+// every kernel-weighted value added straight into the fine grid with a
+// global atomic; Sec. III-B "GM" interpolation reads the fine grid directly.
+// No bin sort: setpts only stores each point's fine-grid cell (packed
+// l1 + n1 (l2 + n2 l3), in the `perm` slot of the parameters) and its
+// fractional position inside the cell (in g1..g3), in the caller's order.
+template <typename T, int DIM>
+__device__ __forceinline__ void unpack_cell(int packed, int n1, int n2, int &l1, int &l2, int &l3) {
+  l1 = packed % n1;
+  const int r = packed / n1;
+  if (DIM == 3) {
+    l2 = r % n2;
+    l3 = r / n2;
+  } else {
+    l2 = r;
+    l3 = 0;
+  }
+}
+
+template <typename T, int DIM, int W>
+__global__ void spread_gmu_kernel(SIParams<T> a, int64_t M) {
+  using C = typename Cplx<T>::type;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M) return;
+  int c1, c2, c3;
+  unpack_cell<T, DIM>(a.perm[i], a.n1, a.n2, c1, c2, c3);
+  const C cv = a.c_in[i];
+  T k1[W], k2[W], k3[W];
+  const int l1 = es_weights<T, W>(a.g1[i], a.beta, k1) + c1;
+  const int l2 = es_weights<T, W>(a.g2[i], a.beta, k2) + c2;
+  int l3 = 0;
+  if (DIM == 3) l3 = es_weights<T, W>(a.g3[i], a.beta, k3) + c3;
+  int x1[W];
+#pragma unroll
+  for (int i1 = 0; i1 < W; i1++) x1[i1] = wrap_once(l1 + i1, a.n1);
+#pragma unroll 1
+  for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+    const T v3 = DIM == 3 ? k3[i3] : T(1);
+    const int64_t z3 = DIM == 3 ? (int64_t)wrap_once(l3 + i3, a.n3) * a.n2 : 0;
+#pragma unroll
+    for (int i2 = 0; i2 < W; i2++) {
+      const T v = k2[i2] * v3;
+      const T vr = cv.x * v, vi = cv.y * v;
+      C *row = a.grid + (z3 + wrap_once(l2 + i2, a.n2)) * (int64_t)a.n1;
+#pragma unroll
+      for (int i1 = 0; i1 < W; i1++) grid_atomic_add(row + x1[i1], vr * k1[i1], vi * k1[i1]);
+    }
+  }
+}
+
+template <typename T, int DIM, int W>
+__global__ void interp_gmu_kernel(SIParams<T> a, int64_t M) {
+  using C = typename Cplx<T>::type;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= M) return;
+  int c1, c2, c3;
+  unpack_cell<T, DIM>(a.perm[i], a.n1, a.n2, c1, c2, c3);
+  T k1[W], k2[W], k3[W];
+  const int l1 = es_weights<T, W>(a.g1[i], a.beta, k1) + c1;
+  const int l2 = es_weights<T, W>(a.g2[i], a.beta, k2) + c2;
+  int l3 = 0;
+  if (DIM == 3) l3 = es_weights<T, W>(a.g3[i], a.beta, k3) + c3;
+  int x1[W];
+#pragma unroll
+  for (int i1 = 0; i1 < W; i1++) x1[i1] = wrap_once(l1 + i1, a.n1);
+  T ar = T(0), ai = T(0);
+#pragma unroll 1
+  for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+    const int64_t z3 = DIM == 3 ? (int64_t)wrap_once(l3 + i3, a.n3) * a.n2 : 0;
+    T sr3 = T(0), si3 = T(0);
+#pragma unroll
+    for (int i2 = 0; i2 < W; i2++) {
+      const C *row = a.grid + (z3 + wrap_once(l2 + i2, a.n2)) * (int64_t)a.n1;
+      T sr = T(0), si = T(0);
+#pragma unroll
+      for (int i1 = 0; i1 < W; i1++) {
+        const C b = __ldg(row + x1[i1]);
+        sr += b.x * k1[i1];
+        si += b.y * k1[i1];
+      }
+      sr3 += sr * k2[i2];
+      si3 += si * k2[i2];
+    }
+    const T v3 = DIM == 3 ? k3[i3] : T(1);
+    ar += sr3 * v3;
+    ai += si3 * v3;
+  }
+  C out;
+  out.x = ar;
+  out.y = ai;
+  a.c_out[i] = out;
+}
+
 // ---------------------------------------------------------------- launchers
 
 template <typename T>
@@ -434,6 +528,12 @@ cudaError_t spread_w(const nufft_plan_s *p, const void *c) {
   SIParams<T> a = make_params<T>(p);
   a.c_in = static_cast<const typename Cplx<T>::type *>(c);
   const unsigned blocks = (unsigned)p->nsub;
+  if (p->method == NUFFT_METHOD_GM) {
+    a.perm = p->bin_of;  // packed cells, caller's order
+    spread_gmu_kernel<T, DIM, W><<<(unsigned)((p->M + p->threads - 1) / p->threads), p->threads, 0,
+                                   p->stream>>>(a, p->M);
+    return cudaGetLastError();
+  }
   if (p->method == NUFFT_METHOD_GM_SORT) {
     spread_gm_kernel<T, DIM, W><<<blocks, p->threads, 0, p->stream>>>(a);
     return cudaGetLastError();
@@ -450,6 +550,12 @@ cudaError_t interp_w(const nufft_plan_s *p, void *c) {
   SIParams<T> a = make_params<T>(p);
   a.c_out = static_cast<typename Cplx<T>::type *>(c);
   const unsigned blocks = (unsigned)p->nsub;
+  if (p->method == NUFFT_METHOD_GM) {
+    a.perm = p->bin_of;  // packed cells, caller's order
+    interp_gmu_kernel<T, DIM, W><<<(unsigned)((p->M + p->threads - 1) / p->threads), p->threads, 0,
+                                   p->stream>>>(a, p->M);
+    return cudaGetLastError();
+  }
   if (p->method == NUFFT_METHOD_GM_SORT) {
     interp_gm_kernel<T, DIM, W><<<blocks, p->threads, 0, p->stream>>>(a);
     return cudaGetLastError();

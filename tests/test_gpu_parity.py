@@ -125,7 +125,7 @@ for _dim, _N in ((2, (100, 70)), (3, (20, 24, 36))):
             T_CASES.append((_dim, _N, _dt, _eps))
 
 
-METHODS = [nf.METHOD_SM, nf.METHOD_GM_SORT, nf.METHOD_REGTILE]
+METHODS = [nf.METHOD_SM, nf.METHOD_GM_SORT, nf.METHOD_REGTILE, nf.METHOD_GM]
 
 
 @pytest.mark.parametrize("cols", [1, 2, 4])
@@ -206,7 +206,8 @@ def test_clustered_points_single_bin(method):
     c = _cplx(M, rng, "f32")
     info = {}
     f = gpu_transform(1, pts, c, (128, 128), 1e-5, -1, "f32", {"method": method}, plan_out=info)
-    assert info["nsub"] >= M // 2048
+    if method != nf.METHOD_GM:  # GM has no subproblems
+        assert info["nsub"] >= M // 2048
     ref = oracle.nufft_type1(pts, c, (128, 128), 1e-5, -1)
     assert oracle.rel_l2(f, ref) <= 1e-5
 
@@ -307,6 +308,15 @@ def test_errors_reported():
 
     finally:
         plan.close()
+
+
+def test_gm_has_no_sort():
+    xs = [torch.zeros(8, device=DEV), torch.zeros(8, device=DEV)]
+    with nf.Plan(1, (8, 8), -1, 1e-5, "complex64", method=nf.METHOD_GM) as plan:
+        plan.setpts(*xs)
+        with pytest.raises(nf.NufftError) as ei:
+            plan.sort()
+        assert ei.value.code == nf.ERR_BAD_OPT
 
 
 def test_plan_reuse_new_strengths_and_points():
