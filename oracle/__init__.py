@@ -118,13 +118,13 @@ def _c128(a) -> np.ndarray:
 
 
 def _coords(pts):
-    """(x, y[, z]) -> (dim, x, y, z-or-None) as contiguous float64 arrays
-    (float32 inputs are converted exactly)."""
+    """(x[, y[, z]]) -> (dim, x, y-or-None, z-or-None) as contiguous float64
+    arrays (float32 inputs are converted exactly)."""
     pts = [_f64(p) for p in pts]
     dim = len(pts)
-    if dim not in (2, 3):
-        raise ValueError("dim must be 2 or 3")
-    return dim, pts[0], pts[1], (pts[2] if dim == 3 else None)
+    if dim not in (1, 2, 3):
+        raise ValueError("dim must be 1, 2 or 3")
+    return dim, pts[0], (pts[1] if dim >= 2 else None), (pts[2] if dim == 3 else None)
 
 
 # --------------------------------------------------------------------------
@@ -217,6 +217,7 @@ def direct_type1(pts, c, N, iflag: int, modes=None, threads: int | None = None) 
     ks = [np.ascontiguousarray(np.asarray(k, dtype=np.int64)) for k in modes]
     if len(ks) != dim:
         raise ValueError("one mode list per dimension")
+    k2 = ks[1] if dim >= 2 else np.zeros(1, np.int64)
     k3 = ks[2] if dim == 3 else np.zeros(1, np.int64)
     shape = tuple(len(k) for k in reversed(ks))
     total = int(np.prod(shape))
@@ -230,10 +231,11 @@ def direct_type1(pts, c, N, iflag: int, modes=None, threads: int | None = None) 
         lo, hi = int(bounds[i]), int(bounds[i + 1])
         if hi <= lo:
             return
+        yy = None if y is None else y[lo:]
         zz = None if z is None else z[lo:]
-        lib.oracle_direct_type1(dim, hi - lo, _ptr(x[lo:]), _ptr(y[lo:]), _ptr(zz),
+        lib.oracle_direct_type1(dim, hi - lo, _ptr(x[lo:]), _ptr(yy), _ptr(zz),
                                 _ptr(c[lo:]), int(iflag), ks[0].size, _ptr(ks[0]),
-                                ks[1].size, _ptr(ks[1]), k3.size, _ptr(k3),
+                                k2.size, _ptr(k2), k3.size, _ptr(k3),
                                 _ptr(parts[i]))
 
     if nthreads == 1:

@@ -53,7 +53,8 @@ static void ksum_add(ksum *s, double vr, double vi) {
 }
 
 /*
- * Type 1 by definition, [cuFINUFFT] Sec. I eq. (1) (and its 3D analogue):
+ * Type 1 by definition, [cuFINUFFT] Sec. I eq. (1) (and its 1D and 3D
+ * analogues, "in the obvious fashion"; y and z are unused in 1D, z in 2D):
  *   f_k = sum_j c_j exp(s i (k1 x_j + k2 y_j + k3 z_j)),  s = +1 if iflag >= 0
  *   else -1 (eq. (1) itself is s = -1),
  * on the tensor grid of modes K1 x K2 (x K3): the nk_i integers listed in
@@ -67,7 +68,8 @@ void oracle_direct_type1(int dim, int64_t M, const double *x, const double *y,
                          const int64_t *k2s, int64_t nk3, const int64_t *k3s,
                          double *f) {
     double s = iflag >= 0 ? 1.0 : -1.0;
-    if (dim == 2) nk3 = 1;
+    if (dim <= 2) nk3 = 1;
+    if (dim == 1) nk2 = 1;
     int64_t nk = nk1 * nk2 * nk3;
     ksum *acc = (ksum *)calloc((size_t)nk, sizeof(ksum));
     double *e1 = (double *)malloc(sizeof(double) * 2 * (size_t)nk1);
@@ -80,7 +82,7 @@ void oracle_direct_type1(int dim, int64_t M, const double *x, const double *y,
             e1[2 * a + 1] = s * sin(ph);
         }
         for (int64_t a = 0; a < nk2; a++) {
-            double ph = (double)k2s[a] * y[j];
+            double ph = dim >= 2 ? (double)k2s[a] * y[j] : 0.0;
             e2[2 * a] = cos(ph);
             e2[2 * a + 1] = s * sin(ph);
         }
@@ -130,7 +132,7 @@ void oracle_direct_type2(int dim, const int64_t *N, const double *x,
                          int iflag, int64_t nt, const int64_t *targets,
                          double *c_out) {
     double s = iflag >= 0 ? 1.0 : -1.0;
-    int64_t N1 = N[0], N2 = N[1], N3 = dim == 3 ? N[2] : 1;
+    int64_t N1 = N[0], N2 = dim >= 2 ? N[1] : 1, N3 = dim == 3 ? N[2] : 1;
     int64_t k1min = -(N1 / 2), k2min = -(N2 / 2), k3min = -(N3 / 2);
     double *e1 = (double *)malloc(sizeof(double) * 2 * (size_t)N1);
     double *e2 = (double *)malloc(sizeof(double) * 2 * (size_t)N2);
@@ -143,7 +145,7 @@ void oracle_direct_type2(int dim, const int64_t *N, const double *x,
             e1[2 * i + 1] = s * sin(ph);
         }
         for (int64_t i = 0; i < N2; i++) {
-            double ph = (double)(k2min + i) * y[j];
+            double ph = dim >= 2 ? (double)(k2min + i) * y[j] : 0.0;
             e2[2 * i] = cos(ph);
             e2[2 * i + 1] = s * sin(ph);
         }
@@ -236,12 +238,15 @@ static int64_t wrap(int64_t l, int64_t n) {
 void oracle_spread(int dim, const int64_t *n, int w, double beta, int64_t M,
                    const double *x, const double *y, const double *z,
                    const double *c, double *b) {
-    int64_t n1 = n[0], n2 = n[1], n3 = dim == 3 ? n[2] : 1;
+    int64_t n1 = n[0], n2 = dim >= 2 ? n[1] : 1, n3 = dim == 3 ? n[2] : 1;
     memset(b, 0, sizeof(double) * 2 * (size_t)(n1 * n2 * n3));
     double k1[32], k2[32], k3[32];
+    int w2 = dim >= 2 ? w : 1;
     for (int64_t j = 0; j < M; j++) {
         int64_t a1 = support(oracle_grid_coord(x[j], n1), w, beta, k1);
-        int64_t a2 = support(oracle_grid_coord(y[j], n2), w, beta, k2);
+        int64_t a2 = 0;
+        k2[0] = 1.0;
+        if (dim >= 2) a2 = support(oracle_grid_coord(y[j], n2), w, beta, k2);
         int64_t a3 = 0;
         int w3 = 1;
         k3[0] = 1.0;
@@ -252,8 +257,8 @@ void oracle_spread(int dim, const int64_t *n, int w, double beta, int64_t M,
         double cr = c[2 * j], ci = c[2 * j + 1];
         for (int t3 = 0; t3 < w3; t3++) {
             int64_t l3 = dim == 3 ? wrap(a3 + t3, n3) : 0;
-            for (int t2 = 0; t2 < w; t2++) {
-                int64_t l2 = wrap(a2 + t2, n2);
+            for (int t2 = 0; t2 < w2; t2++) {
+                int64_t l2 = dim >= 2 ? wrap(a2 + t2, n2) : 0;
                 for (int t1 = 0; t1 < w; t1++) {
                     int64_t l1 = wrap(a1 + t1, n1);
                     double wt = k1[t1] * k2[t2] * k3[t3];
@@ -274,11 +279,14 @@ void oracle_spread(int dim, const int64_t *n, int w, double beta, int64_t M,
 void oracle_interp(int dim, const int64_t *n, int w, double beta, int64_t M,
                    const double *x, const double *y, const double *z,
                    const double *b, double *c) {
-    int64_t n1 = n[0], n2 = n[1], n3 = dim == 3 ? n[2] : 1;
+    int64_t n1 = n[0], n2 = dim >= 2 ? n[1] : 1, n3 = dim == 3 ? n[2] : 1;
     double k1[32], k2[32], k3[32];
+    int w2 = dim >= 2 ? w : 1;
     for (int64_t j = 0; j < M; j++) {
         int64_t a1 = support(oracle_grid_coord(x[j], n1), w, beta, k1);
-        int64_t a2 = support(oracle_grid_coord(y[j], n2), w, beta, k2);
+        int64_t a2 = 0;
+        k2[0] = 1.0;
+        if (dim >= 2) a2 = support(oracle_grid_coord(y[j], n2), w, beta, k2);
         int64_t a3 = 0;
         int w3 = 1;
         k3[0] = 1.0;
@@ -289,8 +297,8 @@ void oracle_interp(int dim, const int64_t *n, int w, double beta, int64_t M,
         double sr = 0.0, si = 0.0;
         for (int t3 = 0; t3 < w3; t3++) {
             int64_t l3 = dim == 3 ? wrap(a3 + t3, n3) : 0;
-            for (int t2 = 0; t2 < w; t2++) {
-                int64_t l2 = wrap(a2 + t2, n2);
+            for (int t2 = 0; t2 < w2; t2++) {
+                int64_t l2 = dim >= 2 ? wrap(a2 + t2, n2) : 0;
                 for (int t1 = 0; t1 < w; t1++) {
                     int64_t l1 = wrap(a1 + t1, n1);
                     double wt = k1[t1] * k2[t2] * k3[t3];
@@ -329,9 +337,9 @@ int64_t oracle_binsort(int dim, const int64_t *n, const int64_t *m, int64_t M,
     for (int64_t b = 0; b < nbins; b++) counts[b] = 0;
     for (int64_t j = 0; j < M; j++) {
         int64_t c1 = (int64_t)floor(oracle_grid_coord(x[j], n[0]));
-        int64_t c2 = (int64_t)floor(oracle_grid_coord(y[j], n[1]));
+        int64_t c2 = dim >= 2 ? (int64_t)floor(oracle_grid_coord(y[j], n[1])) : 0;
         int64_t c3 = dim == 3 ? (int64_t)floor(oracle_grid_coord(z[j], n[2])) : 0;
-        int64_t b1 = c1 / m[0], b2 = c2 / m[1], b3 = dim == 3 ? c3 / m[2] : 0;
+        int64_t b1 = c1 / m[0], b2 = dim >= 2 ? c2 / m[1] : 0, b3 = dim == 3 ? c3 / m[2] : 0;
         int64_t b = b1 + nb[0] * (b2 + nb[1] * b3);
         bin_of[j] = (int32_t)b;
         counts[b]++;
