@@ -36,8 +36,9 @@ METRIC = "NU points/s (type1 & type2, exec excl. setpts) and % of GB300 HBM roof
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = [os.path.join(ROOT, "nonuniform_fft_gb300", "csrc", f)
-                  for f in ("spreadinterp.cuh", "setpts.cu", "nufft_plan.cu")]
+CSRC = os.path.join(ROOT, "nonuniform_fft_gb300", "csrc")
+KERNEL_SOURCES = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                        if f.endswith((".cu", ".cuh")))
 
 
 def parse():
@@ -331,10 +332,11 @@ def run_ours(args, wl):
     achieved = algo[dom] / (per_launch[dom] / 1e3) / 1e9
     spread_kernel = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
                      nf.METHOD_GM: "spread_gmu_kernel",
-                     nf.METHOD_REGTILE: "spread_regtile2d_kernel" if wl.dim == 2
-                     else "spread_plane3d_kernel"}[info["method"]]
+                     nf.METHOD_REGTILE: {1: "spread_reg1d_kernel", 2: "spread_regtile2d_kernel",
+                                         3: "spread_plane3d_kernel"}[wl.dim]}[info["method"]]
     interp_kernel = {nf.METHOD_GM_SORT: "interp_gm_kernel", nf.METHOD_GM: "interp_gmu_kernel"}.get(
-        p2.info()["method"] if has2 else 0, "interp_sm_kernel")
+        p2.info()["method"] if has2 else 0,
+        "interp_sm1d_kernel" if wl.dim == 1 else "interp_sm_kernel")
     kernel_name = {"spread": spread_kernel, "interp": interp_kernel}[dom]
     roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak,

@@ -97,7 +97,7 @@ typedef struct nufft_plan_s *nufft_plan_t;
  * Create a plan.  Defined by Sec. I-A ("plan, setup, execute, destroy") and
  * Sec. II (parameters).
  *   type        1 or 2 (eq. (1) or eq. (3)).
- *   dim         2 or 3.
+ *   dim         1, 2 or 3 (1D: the definitions "in the obvious fashion", Sec. I).
  *   n_modes     host array of dim entries N_1, N_2 (, N_3), each >= 1.
  *   iflag       sign of the exponent: >= 0 -> +1, < 0 -> -1.
  *   eps         requested relative tolerance; sets the kernel width
@@ -117,10 +117,11 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
  * Set a tuning option; takes effect at the next setpts.  Keys:
  *   "method"   NUFFT_METHOD_* (type 1 spreading; type 2 always uses the
  *              tiled shared-memory interpolator unless "method" is GM_SORT).
- *              AUTO picks REGTILE for type 1 and SM for type 2.  REGTILE
+ *              AUTO picks REGTILE for type 1 and SM for type 2 (the only
+ *              methods in 1D; others give BAD_OPT there).  REGTILE
  *              fixes the bin size (the "bin" options are ignored, except
- *              "bin2" in 3D), and type 2 plans with it interpolate with the SM
- *              kernel.
+ *              "bin2" in 3D); it is a spreading method, so a type 2 plan
+ *              given it runs as SM (info "method" then reads SM).
  *   "bin1", "bin2", "bin3"   bin size m_i in fine-grid cells (Sec. III-A), >= 1.
  *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1.
  *   "threads"  threads per block of the SM / GM-sort spreading and
@@ -135,7 +136,7 @@ int nufft_set_opt(nufft_plan_t plan, const char *key, double value);
  * Set the nonuniform points (Sec. III-A bin sort and SM step 1 subproblems).
  *   M        number of points, >= 0 (M = 0 makes execute produce zeros / nothing).
  *   x, y, z  M coordinates each, of the plan's real type; z is ignored (may be
- *            NULL) in 2D.  Host or device pointers.  Read once: the plan keeps
+ *            NULL) in 2D, y and z in 1D.  Host or device pointers.  Read once: the plan keeps
  *            its own sorted, grid-scaled copy, so the caller may free or
  *            overwrite them afterwards.
  * Synchronises the plan's stream once (to size the subproblem table).

@@ -125,7 +125,7 @@ def set_opt(plan: int, key: str, value: float):
     _check(load_library().nufft_set_opt(plan, key.encode(), float(value)), f"set_opt({key})")
 
 
-def setpts(plan: int, M: int, x, y, z=None):
+def setpts(plan: int, M: int, x, y=None, z=None):
     _check(load_library().nufft_setpts(plan, int(M), _ptr(x), _ptr(y), _ptr(z)), "setpts")
 
 
@@ -179,7 +179,7 @@ class Plan:
     def set_opt(self, key: str, value: float):
         set_opt(self.handle, key, value)
 
-    def setpts(self, x, y, z=None):
+    def setpts(self, x, y=None, z=None):
         self.M = int(x.shape[0]) if hasattr(x, "shape") else len(x)
         setpts(self.handle, self.M, x, y, z)
 

@@ -101,7 +101,7 @@ cudaError_t deconv_t(const nufft_plan_s *p, void *f) {
   const unsigned blocks = (unsigned)((total + threads - 1) / threads);
   const T *p1 = (const T *)p->pfac[0], *p2 = (const T *)p->pfac[1];
   const T *p3 = (const T *)(p->dim == 3 ? p->pfac[2] : p->pfac[0]);
-  if (p->dim == 2)
+  if (p->dim <= 2)  // 1D plans carry N2 = n2 = 1 and the factor p2 = 1
     deconvolve_kernel<T, 2><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)p->grid, p1, p2, p3, (C *)f, total);
   else
     deconvolve_kernel<T, 3><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)p->grid, p1, p2, p3, (C *)f, total);
@@ -116,7 +116,7 @@ cudaError_t pad_t(const nufft_plan_s *p, const void *f) {
   const unsigned blocks = (unsigned)((total + threads - 1) / threads);
   const T *p1 = (const T *)p->pfac[0], *p2 = (const T *)p->pfac[1];
   const T *p3 = (const T *)(p->dim == 3 ? p->pfac[2] : p->pfac[0]);
-  if (p->dim == 2)
+  if (p->dim <= 2)
     pad_kernel<T, 2><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)f, p1, p2, p3, (C *)p->grid, total);
   else
     pad_kernel<T, 3><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)f, p1, p2, p3, (C *)p->grid, total);

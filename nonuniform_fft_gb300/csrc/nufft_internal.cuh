@@ -125,6 +125,10 @@ template <typename T>
 cudaError_t launch_spread_plane3d(const nufft_plan_s *p, const void *c);
 void plane3d_bins(int w, int dtype, int *m1, int *m2, int *m3);
 
+// spreadinterp_1d.cu: 1D register-tile spreading and shared-memory interpolation.
+cudaError_t launch_spread_1d(const nufft_plan_s *p, const void *c);
+cudaError_t launch_interp_1d(const nufft_plan_s *p, void *c);
+
 // deconv.cu: type 1 correction + truncation, type 2 correction + padding.
 cudaError_t launch_deconvolve(const nufft_plan_s *p, void *f);
 cudaError_t launch_pad(const nufft_plan_s *p, const void *f);

@@ -223,7 +223,7 @@ const char *nufft_strerror(int code) {
 int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double eps, int dtype,
                    void *cuda_stream, nufft_plan_t *out) {
   if (out) *out = nullptr;
-  if (!out || !n_modes || (type != 1 && type != 2) || (dim != 2 && dim != 3) ||
+  if (!out || !n_modes || (type != 1 && type != 2) || dim < 1 || dim > 3 ||
       (dtype != 0 && dtype != 1))
     return NUFFT_ERR_BAD_ARG;
   for (int d = 0; d < dim; d++)
@@ -262,8 +262,11 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
     if (cudaGetDevice(&p->device) != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
     const size_t rs = real_size(p);
     if (cudaMalloc(&p->grid, (size_t)cells * 2 * rs) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
-    for (int d = 0; d < dim; d++) {
-      std::vector<double> pf = correction_factors(p->N[d], p->n[d], w, p->beta);
+    for (int d = 0; d < 3; d++) {
+      // dimensions beyond dim get the single factor 1, so the 2D correction
+      // kernels serve 1D plans unchanged
+      std::vector<double> pf = d < dim ? correction_factors(p->N[d], p->n[d], w, p->beta)
+                                       : std::vector<double>(1, 1.0);
       if (cudaMalloc(&p->pfac[d], pf.size() * rs) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
       cudaError_t e;
       if (dtype == 0) {
@@ -278,7 +281,9 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
     // cuFFT: row-major dims, slowest first (our x index is fastest)
     cufftResult fr;
     const cufftType ft = dtype == 0 ? CUFFT_C2C : CUFFT_Z2Z;
-    if (dim == 2)
+    if (dim == 1)
+      fr = cufftPlan1d(&p->fft, (int)p->n[0], ft, 1);
+    else if (dim == 2)
       fr = cufftPlan2d(&p->fft, (int)p->n[1], (int)p->n[0], ft);
     else
       fr = cufftPlan3d(&p->fft, (int)p->n[2], (int)p->n[1], (int)p->n[0], ft);
@@ -328,7 +333,8 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
 }
 
 int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const void *z) {
-  if (!p || M < 0 || (M > 0 && (!x || !y || (p->dim == 3 && !z)))) return NUFFT_ERR_BAD_ARG;
+  if (!p || M < 0 || (M > 0 && (!x || (p->dim >= 2 && !y) || (p->dim == 3 && !z))))
+    return NUFFT_ERR_BAD_ARG;
   if (M > (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
   p->have_pts = false;
   if (cudaSetDevice(p->device) != cudaSuccess) return NUFFT_ERR_CUDA;
@@ -337,12 +343,24 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   p->method = p->opt_method;
   if (p->method == NUFFT_METHOD_AUTO)
     p->method = p->type == 1 ? NUFFT_METHOD_REGTILE : NUFFT_METHOD_SM;
+  // the register tile is a spreading scheme: a type 2 plan runs as SM
+  if (p->type == 2 && p->method == NUFFT_METHOD_REGTILE) p->method = NUFFT_METHOD_SM;
+  // 1D: register-tile spreading and shared-memory interpolation only
+  if (p->dim == 1 && p->method != NUFFT_METHOD_REGTILE && p->method != NUFFT_METHOD_SM)
+    return NUFFT_ERR_BAD_OPT;
+  if (p->dim == 1) p->method = p->type == 1 ? NUFFT_METHOD_REGTILE : NUFFT_METHOD_SM;
   int m[3];
   default_bins(p, m);
   for (int d = 0; d < 3; d++)
     if (d < p->dim && p->opt_bin[d] > 0) m[d] = p->opt_bin[d];
   p->regtile_cols = p->opt_regtile_cols > 0 ? p->opt_regtile_cols : 1;
-  if (p->method == NUFFT_METHOD_REGTILE) {
+  if (p->dim == 1) {
+    // one padded-bin column per lane for spreading; long bins for the
+    // interpolator's staged tile, short enough in single precision that the
+    // bin-relative coordinate keeps ~1e-6 cell resolution
+    m[0] = p->type == 1 ? 32 - 2 * ((p->w + 1) / 2) : (p->dtype == 0 ? 128 : 1024);
+    if (p->opt_bin[0] > 0 && p->type == 2) m[0] = p->opt_bin[0];
+  } else if (p->method == NUFFT_METHOD_REGTILE) {
     if (p->dim == 2) {
       nufft::regtile2d_bins(p->w, p->regtile_cols, &m[0], &m[1]);
     } else {
@@ -369,8 +387,8 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   } else if (p->method == NUFFT_METHOD_REGTILE) {
     // a subproblem is one warp (2D) or one block (3D) walking rows in order:
     // cap it so that small problems still spread over every SM
-    const int64_t cap = p->dim == 2 ? 512 : 8192;
-    const int64_t fill = M / (p->dim == 2 ? 152 * 32 : 152 * 4);
+    const int64_t cap = p->dim <= 2 ? 512 : 8192;
+    const int64_t fill = M / (p->dim <= 2 ? 152 * 32 : 152 * 4);
     p->msub = (int)std::max<int64_t>(64, std::min<int64_t>(cap, fill));
   } else {
     p->msub = p->type == 2 ? 2048 : 1024;
@@ -383,7 +401,7 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   p->M = M;
 
   // coordinates in host memory are staged through a device buffer
-  const void *xyz[3] = {x, y, p->dim == 3 ? z : nullptr};
+  const void *xyz[3] = {x, p->dim >= 2 ? y : nullptr, p->dim == 3 ? z : nullptr};
   if (M > 0) {
     const size_t bytes = (size_t)M * real_size(p);
     for (int d = 0; d < p->dim; d++) {
@@ -453,6 +471,7 @@ int nufft_execute(nufft_plan_t p, void *c, void *f) {
   };
   auto spread = [&]() -> cudaError_t {
     if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
+    if (p->dim == 1) return nufft::launch_spread_1d(p, dc);
     if (p->method == NUFFT_METHOD_REGTILE && p->dim == 2)
       return p->dtype == 0 ? nufft::launch_spread_regtile2d<float>(p, dc)
                            : nufft::launch_spread_regtile2d<double>(p, dc);
@@ -465,6 +484,7 @@ int nufft_execute(nufft_plan_t p, void *c, void *f) {
   };
   auto interp = [&]() -> cudaError_t {
     if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
+    if (p->dim == 1) return nufft::launch_interp_1d(p, dc);
     if (p->dim == 2)
       return p->dtype == 0 ? nufft::launch_interp_t<2, float>(p, dc) : nufft::launch_interp_t<2, double>(p, dc);
     return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);

@@ -69,6 +69,10 @@ WORKLOADS = {
                                    1e-6, "f32", (1, 2), "uniform", seed=3),
     "3d_f64_N64_M1e7_mix": Workload("3d_f64_N64_M1e7_mix", 3, (64, 64, 64), 10_000_000,
                                     1e-12, "f64", (1, 2), "mix", sigma=0.1, seed=4),
+    # 1D (a "next" row): double precision at tolerance 1e-3 (w = 4), the
+    # setting of the 1D sweeps in the finufft binsize discussion
+    "1d_f64_N1e6_M1e7": Workload("1d_f64_N1e6_M1e7", 1, (1_000_000,), 10_000_000, 1e-3,
+                                 "f64", (1, 2), "uniform", seed=5),
 }
 
 

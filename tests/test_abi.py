@@ -71,7 +71,7 @@ def _makeplan(lib, type_, dim, modes, iflag, eps, dtype):
 
 @pytest.mark.parametrize("args,code", [
     ((3, 2, [8, 8], -1, 1e-6, 0), nf.ERR_BAD_ARG),       # type
-    ((1, 1, [8], -1, 1e-6, 0), nf.ERR_BAD_ARG),          # dim
+    ((1, 0, [8], -1, 1e-6, 0), nf.ERR_BAD_ARG),          # dim
     ((1, 4, [8, 8, 8, 8], -1, 1e-6, 0), nf.ERR_BAD_ARG),
     ((1, 2, [8, 0], -1, 1e-6, 0), nf.ERR_BAD_ARG),       # N < 1
     ((1, 2, None, -1, 1e-6, 0), nf.ERR_BAD_ARG),         # NULL modes

@@ -86,6 +86,8 @@ def _check_direct(err_gpu, err_o2, eps):
 
 SORT_CASES = [
     # dim, N, M, dist, dt, opts
+    (1, (3000,), 20000, "cluster", "f32", {}),
+    (1, (3000,), 20000, "uniform", "f64", {"msub": 64}),
     (2, (100, 70), 20000, "uniform", "f32", {"msub": 256}),
     (2, (100, 70), 20000, "cluster", "f32", {"msub": 100}),
     (2, (64, 64), 5000, "wild", "f64", {}),
@@ -119,7 +121,7 @@ def test_setpts_integer_results_match_oracle(dim, N, M, dist, dt, opts):
 # ---------------------------------------------------------------- transforms
 
 T_CASES = []
-for _dim, _N in ((2, (100, 70)), (3, (20, 24, 36))):
+for _dim, _N in ((1, (1500,)), (2, (100, 70)), (3, (20, 24, 36))):
     for _dt, _epss in (("f32", (1e-2, 1e-5, 1e-6)), ("f64", (1e-3, 1e-9, 1e-12))):
         for _eps in _epss:
             T_CASES.append((_dim, _N, _dt, _eps))
@@ -146,6 +148,8 @@ def test_regtile_columns_per_lane(cols, dt, eps):
 @pytest.mark.parametrize("method", METHODS)
 @pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
 def test_type1_matches_oracle(dim, N, dt, eps, method):
+    if dim == 1 and method in (nf.METHOD_GM, nf.METHOD_GM_SORT):
+        pytest.skip("1D has the register-tile spreader and the shared-memory interpolator")
     rng = np.random.default_rng(21)
     M = 20000
     pts = _pts(dim, M, "uniform", rng, dt)
@@ -162,8 +166,8 @@ def test_type1_matches_oracle(dim, N, dt, eps, method):
 @pytest.mark.parametrize("method", METHODS)
 @pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
 def test_type2_matches_oracle(dim, N, dt, eps, method):
-    if method == nf.METHOD_REGTILE and dim == 3:
-        pytest.skip("register-tile spreading is 2D")
+    if dim == 1 and method in (nf.METHOD_GM, nf.METHOD_GM_SORT):
+        pytest.skip("1D has the register-tile spreader and the shared-memory interpolator")
     rng = np.random.default_rng(22)
     M = 20000
     pts = _pts(dim, M, "uniform", rng, dt)
@@ -229,7 +233,7 @@ def test_regtile3d_clustered_and_ragged(dt, eps, msub):
     assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, 1)) <= TOL_O2[dt]
 
 
-@pytest.mark.parametrize("N", [(1, 1), (2, 3), (1, 4, 2)])
+@pytest.mark.parametrize("N", [(1,), (3,), (1, 1), (2, 3), (1, 4, 2)])
 def test_tiny_mode_counts(N):
     """Fine grid of 2w points per dimension: the padded tile wraps onto itself."""
     rng = np.random.default_rng(4)
@@ -308,6 +312,14 @@ def test_errors_reported():
 
     finally:
         plan.close()
+
+
+def test_1d_rejects_other_methods():
+    xs = [torch.zeros(8, device=DEV)]
+    with nf.Plan(1, (8,), -1, 1e-5, "complex64", method=nf.METHOD_GM) as plan:
+        with pytest.raises(nf.NufftError) as ei:
+            plan.setpts(*xs)
+        assert ei.value.code == nf.ERR_BAD_OPT
 
 
 def test_gm_has_no_sort():
