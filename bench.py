@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="points per transform in the CPU baseline sample (0: auto)")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="strength vectors per transform (nufft_execute_batch); 1: nufft_execute")
     ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
                     help="plan option for both plans (nufft_set_opt), e.g. msub=1024; repeatable")
     return ap.parse_args()
@@ -90,21 +92,23 @@ def job_throughput(world: int, units_per_step: int, steps: int, t_max_s: float) 
     return world * units_per_step * steps / t_max_s
 
 
-def algorithmic_bytes(wl: W.Workload, n) -> dict:
-    """Minimum bytes each kernel must move per launch (one transform):
-    coordinates (d reals), one complex strength / result and one 4-byte
-    permutation index per point, plus the fine-grid traffic."""
+def algorithmic_bytes(wl: W.Workload, n, nvec: int = 1) -> dict:
+    """Minimum bytes each kernel must move per launch of nvec vectors:
+    coordinates (d reals) and one 4-byte permutation index per point once,
+    and per vector one complex strength / result per point plus the
+    fine-grid traffic."""
     cs = 4 if wl.dtype == "f32" else 8
     cb = 2 * cs
     d = wl.dim
     M = wl.M
     cells = int(np.prod(n))
     modes = int(np.prod(wl.N))
+    v = nvec
     return {
-        "spread": M * (d * cs + cb + 4) + 2 * cells * cb,   # points in; grid read + written
-        "interp": cells * cb + M * (d * cs + 4 + cb),       # grid in; points in, c out
-        "deconv": 2 * modes * cb,
-        "pad": modes * cb + cells * cb,
+        "spread": M * (d * cs + 4) + v * (M * cb + 2 * cells * cb),  # points; c in; grid read + written
+        "interp": M * (d * cs + 4) + v * (cells * cb + M * cb),      # points; grid in, c out
+        "deconv": v * 2 * modes * cb,
+        "pad": v * (modes * cb + cells * cb),
     }
 
 
@@ -257,10 +261,16 @@ def run_ours(args, wl):
     N = wl.N
     with torch.cuda.stream(stream):
         xs = [torch.from_numpy(p).to(dev) for p in pts]
+        B = args.batch
+        # B vectors: the workload's own, then copies rotated by a phase each
         c_in = torch.from_numpy(c_np).to(dev)
         f_in = torch.from_numpy(fk_np).to(dev)
-        f_out = torch.empty(int(np.prod(N)), dtype=ctorch, device=dev)
-        c_out = torch.empty(wl.M, dtype=ctorch, device=dev)
+        if B > 1:
+            ph = torch.exp(1j * torch.arange(B, dtype=torch.float64, device=dev)).to(ctorch)
+            c_in = (ph[:, None] * c_in[None, :]).contiguous()
+            f_in = (ph[:, None] * f_in[None, :]).contiguous()
+        f_out = torch.empty(B * int(np.prod(N)), dtype=ctorch, device=dev)
+        c_out = torch.empty(B * wl.M, dtype=ctorch, device=dev)
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream.synchronize()
     del pts
@@ -278,9 +288,14 @@ def run_ours(args, wl):
     has2 = 2 in wl.types
 
     def step():
-        p1.execute(c_in, f_out)
-        if has2:
-            p2.execute(c_out, f_in)
+        if B == 1:
+            p1.execute(c_in, f_out)
+            if has2:
+                p2.execute(c_out, f_in)
+        else:
+            p1.execute_batch(B, c_in, f_out)
+            if has2:
+                p2.execute_batch(B, c_out, f_in)
 
     for _ in range(args.warmup):
         step()
@@ -313,15 +328,17 @@ def run_ours(args, wl):
         dist.barrier()
     total_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1))
     t_max = reduce_max(total_ms, dev)
-    pts_per_step = wl.M * len(wl.types)
+    pts_per_step = wl.M * len(wl.types) * B
     value = job_throughput(world, pts_per_step, args.steps, t_max / 1e3)
 
     # roofline of the dominant kernel (per-launch averages over the timed region)
     K = args.steps
-    algo = algorithmic_bytes(wl, n)
-    per_launch = {"spread": stage["spread"] / K}
+    vpp = min(B, info["batch"]) if B > 1 else 1       # vectors one launch processes
+    launches = -(-B // vpp)                           # spread / interp launches per transform
+    algo = algorithmic_bytes(wl, n, vpp)
+    per_launch = {"spread": stage["spread"] / (K * launches)}
     if has2:
-        per_launch["interp"] = stage["interp"] / K
+        per_launch["interp"] = stage["interp"] / (K * launches)
     dom = max(per_launch, key=per_launch.get)
     try:
         with open(PEAKS_PATH) as fh:
@@ -347,27 +364,35 @@ def run_ours(args, wl):
     # end to end through the C ABI with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        hc = torch.from_numpy(c_np).pin_memory()
-        hf = torch.from_numpy(fk_np).pin_memory()
-        hf_out = torch.empty(int(np.prod(N)), dtype=ctorch).pin_memory()
-        hc_out = torch.empty(wl.M, dtype=ctorch).pin_memory()
-        p1.execute(hc, hf_out)
-        if has2:
-            p2.execute(hc_out, hf)
+        hc = c_in.cpu().pin_memory()
+        hf = f_in.cpu().pin_memory()
+        hf_out = torch.empty(B * int(np.prod(N)), dtype=ctorch).pin_memory()
+        hc_out = torch.empty(B * wl.M, dtype=ctorch).pin_memory()
+
+        def host_step():
+            # host c in, host f out; host f in, host c out (synchronous calls)
+            if B == 1:
+                p1.execute(hc, hf_out)
+                if has2:
+                    p2.execute(hc_out, hf)
+            else:
+                p1.execute_batch(B, hc, hf_out)
+                if has2:
+                    p2.execute_batch(B, hc_out, hf)
+
+        host_step()
         e2e_steps = max(3, min(args.steps, 10))
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            p1.execute(hc, hf_out)        # host c in, host f out (synchronous)
-            if has2:
-                p2.execute(hc_out, hf)    # host f in, host c out (synchronous)
+            host_step()
         el = reduce_max(time.perf_counter() - t0, dev)
         cb = hc.element_size()
         modes = int(np.prod(N))
         e2e = {"value": job_throughput(world, pts_per_step, e2e_steps, el), "unit": "NU points/s",
-               "h2d_bytes_per_step": wl.M * cb + (modes * cb if has2 else 0),
-               "d2h_bytes_per_step": modes * cb + (wl.M * cb if has2 else 0)}
+               "h2d_bytes_per_step": B * (wl.M * cb + (modes * cb if has2 else 0)),
+               "d2h_bytes_per_step": B * (modes * cb + (wl.M * cb if has2 else 0))}
 
     # timing scopes of [cuFINUFFT] Sec. IV-C: "exec" (the step above), "total"
     # (setpts + exec, on the device) and "total+mem" (host arrays in and out,
@@ -379,10 +404,9 @@ def run_ours(args, wl):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         p1.setpts(*hx)
-        p1.execute(hc, hf_out)
         if has2:
             p2.setpts(*hx)
-            p2.execute(hc_out, hf)
+        host_step()
         torch.cuda.synchronize()
         scopes["total_mem_ms"] = 1e3 * (time.perf_counter() - t0)
 
@@ -407,6 +431,7 @@ def run_ours(args, wl):
                        "msub": info["msub"], "nsub": info["nsub"],
                        "l2": "flushed between timed steps (256 MiB write, untimed)",
                        "plan_options": opts,
+                       "vectors_per_transform": B, "vectors_per_launch": vpp,
                        "parallelism": f"replicas x{world}"},
             "stage_ms_per_step": {k: v / K for k, v in stage.items()},
             "scopes": scopes,
@@ -414,7 +439,7 @@ def run_ours(args, wl):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (4 if has2 else 2) * K,
+            "gpu_launches": (4 if has2 else 2) * launches * K,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

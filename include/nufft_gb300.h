@@ -84,7 +84,8 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_I_BIN3 9
 #define NUFFT_I_MSUB 10            /* points per subproblem cap M_sub */
 #define NUFFT_I_METHOD 11          /* spreading method in use (NUFFT_METHOD_*) */
-#define NUFFT_I_COUNT 12
+#define NUFFT_I_BATCH 12           /* vectors per pass of nufft_execute_batch */
+#define NUFFT_I_COUNT 13
 
 /* Spreading / interpolation methods (option "method"). */
 #define NUFFT_METHOD_AUTO 0
@@ -126,6 +127,9 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
  *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1.
  *   "threads"  threads per block of the SM / GM-sort spreading and
  *              interpolation kernels (multiple of 32, 32..1024).
+ *   "batch"    vectors per pass of nufft_execute_batch, 1..1024 (0: as many
+ *              fine grids as fit in 1 GiB, at most 64).  Takes effect at the
+ *              next execute.
  *   "regtile_cols"  tile columns per lane of the REGTILE spreader: 1, 2 or 4
  *              (0: 1).
  * Errors: BAD_ARG (NULL), BAD_OPT (unknown key or invalid value).
@@ -153,6 +157,25 @@ int nufft_setpts(nufft_plan_t plan, int64_t M, const void *x, const void *y, con
  * Errors: BAD_ARG, NO_POINTS, ALLOC (host staging), CUDA, CUFFT.
  */
 int nufft_execute(nufft_plan_t plan, void *c, void *f);
+
+/*
+ * Run the transform on nvec vectors with the points of the last setpts: the
+ * reuse of sorted points "with new strength vectors" that motivates the
+ * plan/setup/execute interface (cuFINUFFT paper, Sec. I).  Each vector is an
+ * independent transform, exactly as nufft_execute would compute it.
+ *   nvec   number of vectors, >= 0 (0: nothing happens).
+ *   c      nvec * M complex, vector v at c + v M (type 1 input, type 2 output).
+ *   f      nvec * prod N_i complex, vector v at f + v prod N_i.
+ * Vectors go through the device in passes of "batch" vectors (info
+ * NUFFT_I_BATCH): one zeroing / padding pass, one spreading / interpolation
+ * launch, one batched cuFFT and one correction launch per pass, over that
+ * many fine grids (allocated at the first execute that needs them, kept by
+ * the plan).  Host and device pointers as for nufft_execute; host arrays go
+ * through staging buffers of one pass.  Timings: stage times summed over the
+ * passes, NUFFT_T_EXEC from the first pass's start to the last pass's end.
+ * Errors: BAD_ARG, NO_POINTS, ALLOC (fine grids, staging), CUDA, CUFFT.
+ */
+int nufft_execute_batch(nufft_plan_t plan, int64_t nvec, void *c, void *f);
 
 /* Release every resource of the plan (NULL is accepted).  Synchronises the
  * plan's stream first.  Errors: CUDA. */

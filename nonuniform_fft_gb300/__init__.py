@@ -20,7 +20,7 @@ import os
 from ._build import LIB_PATH
 
 __all__ = [
-    "makeplan", "set_opt", "setpts", "execute", "destroy", "get_timings", "get_info",
+    "makeplan", "set_opt", "setpts", "execute", "execute_batch", "destroy", "get_timings", "get_info",
     "get_sort", "strerror", "Plan", "NufftError", "load_library", "TIMING_KEYS", "INFO_KEYS",
 ]
 
@@ -30,7 +30,8 @@ ERR_BAD_ARG, ERR_BAD_EPS, ERR_ALLOC, ERR_CUDA, ERR_CUFFT = 1, 2, 3, 4, 5
 ERR_NO_POINTS, ERR_BAD_POINTS, ERR_BAD_OPT, ERR_TOO_LARGE = 6, 7, 8, 9
 METHOD_AUTO, METHOD_SM, METHOD_GM_SORT, METHOD_REGTILE, METHOD_GM = 0, 1, 2, 3, 4
 TIMING_KEYS = ("spread_interp", "fft", "deconv_pad", "zero", "exec", "setpts")
-INFO_KEYS = ("w", "n1", "n2", "n3", "M", "nbins", "nsub", "bin1", "bin2", "bin3", "msub", "method")
+INFO_KEYS = ("w", "n1", "n2", "n3", "M", "nbins", "nsub", "bin1", "bin2", "bin3", "msub", "method",
+             "batch")
 
 _lib = None
 
@@ -57,6 +58,7 @@ def load_library(path: str | None = None):
     lib.nufft_set_opt.argtypes = [P, ctypes.c_char_p, D]
     lib.nufft_setpts.argtypes = [P, I64, P, P, P]
     lib.nufft_execute.argtypes = [P, P, P]
+    lib.nufft_execute_batch.argtypes = [P, I64, P, P]
     lib.nufft_destroy.argtypes = [P]
     lib.nufft_get_timings.argtypes = [P, ctypes.POINTER(D), I]
     lib.nufft_get_info.argtypes = [P, ctypes.POINTER(I64), I]
@@ -64,7 +66,8 @@ def load_library(path: str | None = None):
     lib.nufft_strerror.argtypes = [I]
     lib.nufft_strerror.restype = ctypes.c_char_p
     for name in ("nufft_makeplan", "nufft_set_opt", "nufft_setpts", "nufft_execute",
-                 "nufft_destroy", "nufft_get_timings", "nufft_get_info", "nufft_get_sort"):
+                 "nufft_execute_batch", "nufft_destroy", "nufft_get_timings", "nufft_get_info",
+                 "nufft_get_sort"):
         getattr(lib, name).restype = I
     _lib = lib
     return lib
@@ -133,6 +136,11 @@ def execute(plan: int, c, f):
     _check(load_library().nufft_execute(plan, _ptr(c), _ptr(f)), "execute")
 
 
+def execute_batch(plan: int, nvec: int, c, f):
+    """nufft_execute_batch: nvec vectors stored back to back in c and f."""
+    _check(load_library().nufft_execute_batch(plan, int(nvec), _ptr(c), _ptr(f)), "execute_batch")
+
+
 def destroy(plan: int):
     _check(load_library().nufft_destroy(plan), "destroy")
 
@@ -185,6 +193,9 @@ class Plan:
 
     def execute(self, c, f):
         execute(self.handle, c, f)
+
+    def execute_batch(self, nvec: int, c, f):
+        execute_batch(self.handle, nvec, c, f)
 
     def timings(self) -> dict:
         return get_timings(self.handle)

@@ -32,9 +32,11 @@ __device__ __forceinline__ int fine_of_mode(int i, int half, int n) {
 template <typename T, int DIM>
 __global__ void deconvolve_kernel(ModeGeom g, const typename C2<T>::type *grid, const T *p1,
                                   const T *p2, const T *p3, typename C2<T>::type *f,
-                                  int64_t total) {
+                                  int64_t total, int64_t gstride) {
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
+  grid += blockIdx.y * gstride;  // vector blockIdx.y of a batched launch
+  f += blockIdx.y * total;
   const int i1 = (int)(idx % g.N[0]);
   const int64_t r = idx / g.N[0];
   const int i2 = (int)(r % g.N[1]);
@@ -60,9 +62,12 @@ __device__ __forceinline__ int mode_of_fine(int l, int N, int half, int n) {
 
 template <typename T, int DIM>
 __global__ void pad_kernel(ModeGeom g, const typename C2<T>::type *f, const T *p1, const T *p2,
-                           const T *p3, typename C2<T>::type *grid, int64_t total) {
+                           const T *p3, typename C2<T>::type *grid, int64_t total,
+                           int64_t fstride) {
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
+  f += blockIdx.y * fstride;  // vector blockIdx.y of a batched launch
+  grid += blockIdx.y * total;
   const int l1 = (int)(idx % g.n[0]);
   const int64_t r = idx / g.n[0];
   const int l2 = (int)(r % g.n[1]);
@@ -102,9 +107,11 @@ cudaError_t deconv_t(const nufft_plan_s *p, void *f) {
   const T *p1 = (const T *)p->pfac[0], *p2 = (const T *)p->pfac[1];
   const T *p3 = (const T *)(p->dim == 3 ? p->pfac[2] : p->pfac[0]);
   if (p->dim <= 2)  // 1D plans carry N2 = n2 = 1 and the factor p2 = 1
-    deconvolve_kernel<T, 2><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)p->grid, p1, p2, p3, (C *)f, total);
+    deconvolve_kernel<T, 2><<<dim3(blocks, p->nvec), threads, 0, p->stream>>>(
+        mode_geom(p), (const C *)p->grid, p1, p2, p3, (C *)f, total, grid_cells(p));
   else
-    deconvolve_kernel<T, 3><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)p->grid, p1, p2, p3, (C *)f, total);
+    deconvolve_kernel<T, 3><<<dim3(blocks, p->nvec), threads, 0, p->stream>>>(
+        mode_geom(p), (const C *)p->grid, p1, p2, p3, (C *)f, total, grid_cells(p));
   return cudaGetLastError();
 }
 
@@ -117,9 +124,11 @@ cudaError_t pad_t(const nufft_plan_s *p, const void *f) {
   const T *p1 = (const T *)p->pfac[0], *p2 = (const T *)p->pfac[1];
   const T *p3 = (const T *)(p->dim == 3 ? p->pfac[2] : p->pfac[0]);
   if (p->dim <= 2)
-    pad_kernel<T, 2><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)f, p1, p2, p3, (C *)p->grid, total);
+    pad_kernel<T, 2><<<dim3(blocks, p->nvec), threads, 0, p->stream>>>(
+        mode_geom(p), (const C *)f, p1, p2, p3, (C *)p->grid, total, mode_count(p));
   else
-    pad_kernel<T, 3><<<blocks, threads, 0, p->stream>>>(mode_geom(p), (const C *)f, p1, p2, p3, (C *)p->grid, total);
+    pad_kernel<T, 3><<<dim3(blocks, p->nvec), threads, 0, p->stream>>>(
+        mode_geom(p), (const C *)f, p1, p2, p3, (C *)p->grid, total, mode_count(p));
   return cudaGetLastError();
 }
 

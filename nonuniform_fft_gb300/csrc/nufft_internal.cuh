@@ -6,6 +6,8 @@
 #include <cufft.h>
 
 #include <cstdint>
+#include <utility>
+#include <vector>
 
 #include "../../include/nufft_gb300.h"
 
@@ -46,6 +48,7 @@ struct nufft_plan_s {
   int opt_msub = 0;            // 0: default
   int opt_threads = 0;         // 0: default
   int opt_regtile_cols = 0;    // 0: default
+  int opt_batch = 0;           // vectors per pass of a batched execute (0: default)
 
   // --- resolved at setpts ------------------------------------------------
   int method = NUFFT_METHOD_SM;
@@ -58,9 +61,11 @@ struct nufft_plan_s {
   int64_t nsub = 0;
   int64_t M = 0;
   bool have_pts = false;
+  int nvec = 1;                // vectors in the pass being launched (blockIdx.y range)
 
   // --- device memory ----------------------------------------------------
-  void *grid = nullptr;            // fine grid, n1 n2 n3 complex, x fastest
+  void *grid = nullptr;            // grid_vecs fine grids, each n1 n2 n3 complex, x fastest
+  int64_t grid_vecs = 0;
   void *pfac[3] = {nullptr, nullptr, nullptr};  // correction factors p_i(k), N_i reals
   int32_t *bin_counts = nullptr;   // nbins + 1
   int32_t *bin_starts = nullptr;   // nbins + 1 (last entry: M)
@@ -82,16 +87,20 @@ struct nufft_plan_s {
   void *stage_c = nullptr;         // staging for host c
   int64_t cap_stage_c = 0;
   void *stage_f = nullptr;         // staging for host f
+  int64_t cap_stage_f = 0;
   void *stage_xyz = nullptr;       // staging for host coordinates (3 M reals)
   int64_t cap_stage_xyz = 0;
 
   cufftHandle fft = 0;
   bool fft_made = false;
+  std::vector<std::pair<int, cufftHandle>> fft_many;  // batched plans by vector count
 
   // --- timing -------------------------------------------------------------
   cudaEvent_t ev[8] = {};
   bool ev_made = false;
   bool exec_recorded = false;
+  std::vector<cudaEvent_t> xev;   // execute: 5 events per pass
+  int xpasses = 0;                 // passes of the last execute
   bool setpts_recorded = false;
 };
 

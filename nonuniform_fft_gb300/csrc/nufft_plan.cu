@@ -185,6 +185,8 @@ void release(nufft_plan_s *p) {
   cudaFree(p->stage_f);
   cudaFree(p->stage_xyz);
   if (p->fft_made) cufftDestroy(p->fft);
+  for (auto &h : p->fft_many) cufftDestroy(h.second);
+  for (auto &e : p->xev) cudaEventDestroy(e);
   if (p->ev_made)
     for (auto &e : p->ev) cudaEventDestroy(e);
 }
@@ -195,8 +197,45 @@ int cuda_code(cudaError_t e) {
   return NUFFT_ERR_CUDA;
 }
 
-// Event slots.
-enum { EV_A = 0, EV_B, EV_C, EV_D, EV_E, EV_SET0 = 6, EV_SET1 = 7 };
+// Event slots: setpts in ev[]; execute uses kPassEvents per pass in xev
+// (type 1: zero, spread, FFT, deconvolve, end; type 2: pad, FFT, interp, end).
+enum { EV_SET0 = 6, EV_SET1 = 7 };
+constexpr int kPassEvents = 5;
+
+// Vectors per pass of a batched execute: the "batch" option, else as many
+// fine grids as fit in 1 GiB (at least 1, at most 64).
+int64_t batch_pass(const nufft_plan_s *p) {
+  if (p->opt_batch > 0) return p->opt_batch;
+  const int64_t grid_bytes = nufft::grid_cells(p) * 2 * (int64_t)nufft::real_size(p);
+  return std::max<int64_t>(1, std::min<int64_t>(64, (int64_t(1) << 30) / grid_bytes));
+}
+
+// cuFFT plan transforming nv consecutive fine grids.
+int fft_plan_for(nufft_plan_s *p, int nv, cufftHandle *out) {
+  if (nv == 1) {
+    *out = p->fft;
+    return NUFFT_OK;
+  }
+  for (auto &h : p->fft_many)
+    if (h.first == nv) {
+      *out = h.second;
+      return NUFFT_OK;
+    }
+  int dims[3];
+  for (int d = 0; d < p->dim; d++) dims[d] = (int)p->n[p->dim - 1 - d];  // slowest first
+  const int dist = (int)nufft::grid_cells(p);
+  cufftHandle h;
+  const cufftResult r = cufftPlanMany(&h, p->dim, dims, nullptr, 1, dist, nullptr, 1, dist,
+                                      p->dtype == 0 ? CUFFT_C2C : CUFFT_Z2Z, nv);
+  if (r != CUFFT_SUCCESS) return r == CUFFT_ALLOC_FAILED ? NUFFT_ERR_ALLOC : NUFFT_ERR_CUFFT;
+  if (cufftSetStream(h, p->stream) != CUFFT_SUCCESS) {
+    cufftDestroy(h);
+    return NUFFT_ERR_CUFFT;
+  }
+  p->fft_many.emplace_back(nv, h);
+  *out = h;
+  return NUFFT_OK;
+}
 
 }  // namespace
 
@@ -262,6 +301,7 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
     if (cudaGetDevice(&p->device) != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
     const size_t rs = real_size(p);
     if (cudaMalloc(&p->grid, (size_t)cells * 2 * rs) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
+    p->grid_vecs = 1;
     for (int d = 0; d < 3; d++) {
       // dimensions beyond dim get the single factor 1, so the 2D correction
       // kernels serve 1D plans unchanged
@@ -320,6 +360,9 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
   } else if (!std::strcmp(key, "msub")) {
     if (v < 0 || v > (int64_t(1) << 24)) return NUFFT_ERR_BAD_OPT;
     p->opt_msub = (int)v;
+  } else if (!std::strcmp(key, "batch")) {
+    if (v != 0 && (v < 1 || v > 1024 || v != (double)(int)v)) return NUFFT_ERR_BAD_OPT;
+    p->opt_batch = (int)v;
   } else if (!std::strcmp(key, "regtile_cols")) {
     if (v != 0 && v != 1 && v != 2 && v != 4) return NUFFT_ERR_BAD_OPT;
     p->opt_regtile_cols = (int)v;
@@ -431,101 +474,122 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   return NUFFT_OK;
 }
 
-int nufft_execute(nufft_plan_t p, void *c, void *f) {
-  if (!p) return NUFFT_ERR_BAD_ARG;
+int nufft_execute(nufft_plan_t p, void *c, void *f) { return nufft_execute_batch(p, 1, c, f); }
+
+int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
+  if (!p || nvec < 0) return NUFFT_ERR_BAD_ARG;
   if (!p->have_pts) return NUFFT_ERR_NO_POINTS;
+  if (nvec == 0) return NUFFT_OK;
   if (!f || (p->M > 0 && !c)) return NUFFT_ERR_BAD_ARG;
   if (cudaSetDevice(p->device) != cudaSuccess) return NUFFT_ERR_CUDA;
   cudaStream_t s = p->stream;
   const size_t cb = 2 * real_size(p);
-  const size_t c_bytes = (size_t)p->M * cb, f_bytes = (size_t)nufft::mode_count(p) * cb;
+  const int64_t cells = nufft::grid_cells(p), modes = nufft::mode_count(p);
+  const size_t c_bytes = (size_t)p->M * cb, f_bytes = (size_t)modes * cb;
+  const int64_t pass = std::min<int64_t>(nvec, batch_pass(p));
+  const int64_t npass = (nvec + pass - 1) / pass;
 
-  // stage host arrays
   bool ok = true;
   const bool c_host = p->M > 0 && !is_device_ptr(c, p->device, &ok);
   if (!ok) return NUFFT_ERR_BAD_ARG;
   const bool f_host = !is_device_ptr(f, p->device, &ok);
   if (!ok) return NUFFT_ERR_BAD_ARG;
-  void *dc = c, *df = f;
-  int rc;
-  if (c_host) {
-    if ((rc = grow_buffer(&p->stage_c, &p->cap_stage_c, (int64_t)c_bytes))) return rc;
-    dc = p->stage_c;
-    if (p->type == 1 && cudaMemcpyAsync(dc, c, c_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return NUFFT_ERR_CUDA;
+  int rc = NUFFT_OK;
+  if (c_host && (rc = grow_buffer(&p->stage_c, &p->cap_stage_c, (int64_t)(pass * c_bytes)))) return rc;
+  if (f_host && (rc = grow_buffer(&p->stage_f, &p->cap_stage_f, (int64_t)(pass * f_bytes)))) return rc;
+  // fine grids for one pass (the old ones are freed only once the new fit)
+  if (p->grid_vecs < pass) {
+    void *g = nullptr;
+    if (cudaMalloc(&g, (size_t)(pass * cells) * cb) != cudaSuccess) {
+      cudaGetLastError();
+      return NUFFT_ERR_ALLOC;
+    }
+    cudaFree(p->grid);
+    p->grid = g;
+    p->grid_vecs = pass;
   }
-  if (f_host) {
-    if (!p->stage_f && cudaMalloc(&p->stage_f, f_bytes) != cudaSuccess) return NUFFT_ERR_ALLOC;
-    df = p->stage_f;
-    if (p->type == 2 && cudaMemcpyAsync(df, f, f_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return NUFFT_ERR_CUDA;
+  while ((int64_t)p->xev.size() < npass * kPassEvents) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return NUFFT_ERR_CUDA;
+    p->xev.push_back(e);
   }
 
   const int dir = p->iflag >= 0 ? CUFFT_INVERSE : CUFFT_FORWARD;
-  auto fft = [&]() -> int {
-    cufftResult r = p->dtype == 0
-                        ? cufftExecC2C(p->fft, (cufftComplex *)p->grid, (cufftComplex *)p->grid, dir)
-                        : cufftExecZ2Z(p->fft, (cufftDoubleComplex *)p->grid,
-                                       (cufftDoubleComplex *)p->grid, dir);
-    return r == CUFFT_SUCCESS ? NUFFT_OK : NUFFT_ERR_CUFFT;
-  };
-  auto spread = [&]() -> cudaError_t {
-    if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
-    if (p->dim == 1) return nufft::launch_spread_1d(p, dc);
-    if (p->method == NUFFT_METHOD_REGTILE && p->dim == 2)
-      return p->dtype == 0 ? nufft::launch_spread_regtile2d<float>(p, dc)
-                           : nufft::launch_spread_regtile2d<double>(p, dc);
-    if (p->method == NUFFT_METHOD_REGTILE)
-      return p->dtype == 0 ? nufft::launch_spread_plane3d<float>(p, dc)
-                           : nufft::launch_spread_plane3d<double>(p, dc);
-    if (p->dim == 2)
-      return p->dtype == 0 ? nufft::launch_spread_t<2, float>(p, dc) : nufft::launch_spread_t<2, double>(p, dc);
-    return p->dtype == 0 ? nufft::launch_spread_t<3, float>(p, dc) : nufft::launch_spread_t<3, double>(p, dc);
-  };
-  auto interp = [&]() -> cudaError_t {
-    if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
-    if (p->dim == 1) return nufft::launch_interp_1d(p, dc);
-    if (p->dim == 2)
-      return p->dtype == 0 ? nufft::launch_interp_t<2, float>(p, dc) : nufft::launch_interp_t<2, double>(p, dc);
-    return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);
-  };
-
-  cudaError_t e;
-  if (p->type == 1) {
-    // zero -> spread (eq. (7)) -> FFT (eq. (9)) -> correct + truncate (eq. (10))
-    if ((e = cudaEventRecord(p->ev[EV_A], s)) != cudaSuccess) return cuda_code(e);
-    if ((e = cudaMemsetAsync(p->grid, 0, (size_t)nufft::grid_cells(p) * cb, s)) != cudaSuccess) return cuda_code(e);
-    if ((e = cudaEventRecord(p->ev[EV_B], s)) != cudaSuccess) return cuda_code(e);
-    if ((e = spread()) != cudaSuccess) return cuda_code(e);
-    if ((e = cudaEventRecord(p->ev[EV_C], s)) != cudaSuccess) return cuda_code(e);
-    if ((rc = fft())) return rc;
-    if ((e = cudaEventRecord(p->ev[EV_D], s)) != cudaSuccess) return cuda_code(e);
-    if ((e = nufft::launch_deconvolve(p, df)) != cudaSuccess) return cuda_code(e);
-    if ((e = cudaEventRecord(p->ev[EV_E], s)) != cudaSuccess) return cuda_code(e);
-  } else {
-    // correct + pad (eq. (11)) -> FFT (eq. (12)) -> interpolate (Sec. II-B c)
-    if ((e = cudaEventRecord(p->ev[EV_A], s)) != cudaSuccess) return cuda_code(e);
-    if (p->M > 0) {
-      if ((e = nufft::launch_pad(p, df)) != cudaSuccess) return cuda_code(e);
+  p->exec_recorded = false;
+  cudaError_t e = cudaSuccess;
+  for (int64_t k = 0; k < npass; k++) {
+    const int64_t v0 = k * pass, nv = std::min<int64_t>(pass, nvec - v0);
+    char *cu = static_cast<char *>(c) + (c ? v0 * c_bytes : 0);  // caller's arrays of this pass
+    char *fu = static_cast<char *>(f) + v0 * f_bytes;
+    void *dc = c_host ? p->stage_c : cu, *df = f_host ? p->stage_f : fu;
+    if (p->type == 1 && c_host && cudaMemcpyAsync(dc, cu, nv * c_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
+    if (p->type == 2 && f_host && cudaMemcpyAsync(df, fu, nv * f_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
+    cufftHandle plan_fft;
+    if ((rc = fft_plan_for(p, (int)nv, &plan_fft))) return rc;
+    p->nvec = (int)nv;
+    cudaEvent_t *ev = &p->xev[k * kPassEvents];
+    auto fft = [&]() -> int {
+      cufftResult r = p->dtype == 0
+                          ? cufftExecC2C(plan_fft, (cufftComplex *)p->grid, (cufftComplex *)p->grid, dir)
+                          : cufftExecZ2Z(plan_fft, (cufftDoubleComplex *)p->grid,
+                                         (cufftDoubleComplex *)p->grid, dir);
+      return r == CUFFT_SUCCESS ? NUFFT_OK : NUFFT_ERR_CUFFT;
+    };
+    auto spread = [&]() -> cudaError_t {
+      if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
+      if (p->dim == 1) return nufft::launch_spread_1d(p, dc);
+      if (p->method == NUFFT_METHOD_REGTILE && p->dim == 2)
+        return p->dtype == 0 ? nufft::launch_spread_regtile2d<float>(p, dc)
+                             : nufft::launch_spread_regtile2d<double>(p, dc);
+      if (p->method == NUFFT_METHOD_REGTILE)
+        return p->dtype == 0 ? nufft::launch_spread_plane3d<float>(p, dc)
+                             : nufft::launch_spread_plane3d<double>(p, dc);
+      if (p->dim == 2)
+        return p->dtype == 0 ? nufft::launch_spread_t<2, float>(p, dc) : nufft::launch_spread_t<2, double>(p, dc);
+      return p->dtype == 0 ? nufft::launch_spread_t<3, float>(p, dc) : nufft::launch_spread_t<3, double>(p, dc);
+    };
+    auto interp = [&]() -> cudaError_t {
+      if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
+      if (p->dim == 1) return nufft::launch_interp_1d(p, dc);
+      if (p->dim == 2)
+        return p->dtype == 0 ? nufft::launch_interp_t<2, float>(p, dc) : nufft::launch_interp_t<2, double>(p, dc);
+      return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);
+    };
+    if (p->type == 1) {
+      // zero -> spread (eq. (7)) -> FFT (eq. (9)) -> correct + truncate (eq. (10))
+      if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess ||
+          (e = cudaMemsetAsync(p->grid, 0, (size_t)(nv * cells) * cb, s)) != cudaSuccess ||
+          (e = cudaEventRecord(ev[1], s)) != cudaSuccess || (e = spread()) != cudaSuccess ||
+          (e = cudaEventRecord(ev[2], s)) != cudaSuccess)
+        break;
+      if ((rc = fft())) break;
+      if ((e = cudaEventRecord(ev[3], s)) != cudaSuccess || (e = nufft::launch_deconvolve(p, df)) != cudaSuccess ||
+          (e = cudaEventRecord(ev[4], s)) != cudaSuccess)
+        break;
+    } else {
+      // correct + pad (eq. (11)) -> FFT (eq. (12)) -> interpolate (Sec. II-B c)
+      if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess) break;
+      if (p->M > 0 && (e = nufft::launch_pad(p, df)) != cudaSuccess) break;
+      if ((e = cudaEventRecord(ev[1], s)) != cudaSuccess) break;
+      if (p->M > 0 && (rc = fft())) break;
+      if ((e = cudaEventRecord(ev[2], s)) != cudaSuccess || (e = interp()) != cudaSuccess ||
+          (e = cudaEventRecord(ev[3], s)) != cudaSuccess)
+        break;
     }
-    if ((e = cudaEventRecord(p->ev[EV_B], s)) != cudaSuccess) return cuda_code(e);
-    if (p->M > 0 && (rc = fft())) return rc;
-    if ((e = cudaEventRecord(p->ev[EV_C], s)) != cudaSuccess) return cuda_code(e);
-    if ((e = interp()) != cudaSuccess) return cuda_code(e);
-    if ((e = cudaEventRecord(p->ev[EV_D], s)) != cudaSuccess) return cuda_code(e);
+    // host results of this pass
+    if (p->type == 1 && f_host && cudaMemcpyAsync(fu, df, nv * f_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
+    if (p->type == 2 && c_host && cudaMemcpyAsync(cu, dc, nv * c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
+    p->xpasses = (int)(k + 1);
   }
+  p->nvec = 1;
+  if (rc) return rc;
+  if (e != cudaSuccess) return cuda_code(e);
   p->exec_recorded = true;
-
-  // copy host results back and wait for them
-  if (p->type == 1 && f_host) {
-    if (cudaMemcpyAsync(f, df, f_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NUFFT_ERR_CUDA;
-  }
-  if (p->type == 2 && c_host) {
-    if (cudaMemcpyAsync(c, dc, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NUFFT_ERR_CUDA;
-  }
-  if (c_host || f_host) {
-    if (cudaStreamSynchronize(s) != cudaSuccess) return NUFFT_ERR_CUDA;
-  }
+  if ((c_host || f_host) && cudaStreamSynchronize(s) != cudaSuccess) return NUFFT_ERR_CUDA;
   return NUFFT_OK;
 }
 
@@ -541,35 +605,35 @@ int nufft_destroy(nufft_plan_t p) {
 int nufft_get_timings(nufft_plan_t p, double *ms, int n) {
   if (!p || !ms || n < 0) return NUFFT_ERR_BAD_ARG;
   double t[NUFFT_T_COUNT] = {0, 0, 0, 0, 0, 0};
-  auto span = [&](int a, int b, double *dst) -> int {
+  auto span = [&](cudaEvent_t a, cudaEvent_t b, double *dst) -> int {
     float v = 0;
-    if (cudaEventSynchronize(p->ev[b]) != cudaSuccess) return NUFFT_ERR_CUDA;
-    if (cudaEventElapsedTime(&v, p->ev[a], p->ev[b]) != cudaSuccess) return NUFFT_ERR_CUDA;
-    *dst = v;
+    if (cudaEventSynchronize(b) != cudaSuccess) return NUFFT_ERR_CUDA;
+    if (cudaEventElapsedTime(&v, a, b) != cudaSuccess) return NUFFT_ERR_CUDA;
+    *dst += v;
     return NUFFT_OK;
   };
   int rc;
   if (p->exec_recorded) {
-    if (p->type == 1) {
-      if ((rc = span(EV_A, EV_B, &t[NUFFT_T_ZERO])) || (rc = span(EV_B, EV_C, &t[NUFFT_T_SPREAD_INTERP])) ||
-          (rc = span(EV_C, EV_D, &t[NUFFT_T_FFT])) || (rc = span(EV_D, EV_E, &t[NUFFT_T_DECONV_PAD])) ||
-          (rc = span(EV_A, EV_E, &t[NUFFT_T_EXEC])))
-        return rc;
-    } else {
-      if ((rc = span(EV_A, EV_B, &t[NUFFT_T_DECONV_PAD])) || (rc = span(EV_B, EV_C, &t[NUFFT_T_FFT])) ||
-          (rc = span(EV_C, EV_D, &t[NUFFT_T_SPREAD_INTERP])) || (rc = span(EV_A, EV_D, &t[NUFFT_T_EXEC])))
-        return rc;
+    // stage times summed over the passes of the last execute
+    const int last = p->type == 1 ? 4 : 3;
+    const int stage[2][4] = {{NUFFT_T_ZERO, NUFFT_T_SPREAD_INTERP, NUFFT_T_FFT, NUFFT_T_DECONV_PAD},
+                             {NUFFT_T_DECONV_PAD, NUFFT_T_FFT, NUFFT_T_SPREAD_INTERP, -1}};
+    for (int k = 0; k < p->xpasses; k++) {
+      cudaEvent_t *ev = &p->xev[k * kPassEvents];
+      for (int i = 0; i < last; i++)
+        if ((rc = span(ev[i], ev[i + 1], &t[stage[p->type - 1][i]]))) return rc;
     }
+    if ((rc = span(p->xev[0], p->xev[(p->xpasses - 1) * kPassEvents + last], &t[NUFFT_T_EXEC]))) return rc;
   }
-  if (p->setpts_recorded && (rc = span(EV_SET0, EV_SET1, &t[NUFFT_T_SETPTS]))) return rc;
+  if (p->setpts_recorded && (rc = span(p->ev[EV_SET0], p->ev[EV_SET1], &t[NUFFT_T_SETPTS]))) return rc;
   for (int i = 0; i < n && i < NUFFT_T_COUNT; i++) ms[i] = t[i];
   return NUFFT_OK;
 }
 
 int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
   if (!p || !info || n < 0) return NUFFT_ERR_BAD_ARG;
-  const int64_t v[NUFFT_I_COUNT] = {p->w,     p->n[0],  p->n[1],  p->n[2], p->M,    p->nbins,
-                                    p->nsub,  p->m[0],  p->m[1],  p->m[2], p->msub, p->method};
+  const int64_t v[NUFFT_I_COUNT] = {p->w,    p->n[0], p->n[1], p->n[2], p->M,      p->nbins,  p->nsub,
+                                    p->m[0], p->m[1], p->m[2], p->msub, p->method, batch_pass(p)};
   for (int i = 0; i < n && i < NUFFT_I_COUNT; i++) info[i] = v[i];
   return NUFFT_OK;
 }

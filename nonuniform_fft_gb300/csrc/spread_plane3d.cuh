@@ -60,6 +60,7 @@ struct Plane3DParams {
   int n1, n2, n3;
   int m1, m2, m3;
   int nb1, nb2;
+  int64_t cstride, gstride;  // per vector: M strengths, one fine grid
 };
 
 template <typename T, int W, int Z, int K>
@@ -67,6 +68,8 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
     spread_plane3d_kernel(Plane3DParams<T> a) {
   using G = Plane3D<T, W, Z, K>;
   using CT = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
   __shared__ __align__(16) T s_wy[G::S][G::WXP];
   __shared__ __align__(16) T s_wz[G::S][G::WXP];
   __shared__ T s_wx[G::S][G::WX];
@@ -245,7 +248,7 @@ template <typename T, int W>
 cudaError_t spread_plane3d_w(const nufft_plan_s *p, const void *c) {
   using Ch = Plane3DChoice<T, W>;
   using G = Plane3D<T, W, Ch::Z, Ch::K>;
-  Plane3DParams<T> a;
+  Plane3DParams<T> a{};
   a.sub = p->subprob;
   a.perm = p->perm;
   a.g1 = static_cast<const T *>(p->gcoord[0]);
@@ -263,7 +266,9 @@ cudaError_t spread_plane3d_w(const nufft_plan_s *p, const void *c) {
   a.m3 = p->m[2];
   a.nb1 = p->nb[0];
   a.nb2 = p->nb[1];
-  spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<(unsigned)p->nsub, G::THREADS, 0, p->stream>>>(a);
+  a.cstride = p->M;
+  a.gstride = grid_cells(p);
+  spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<dim3((unsigned)p->nsub, p->nvec), G::THREADS, 0, p->stream>>>(a);
   return cudaGetLastError();
 }
 

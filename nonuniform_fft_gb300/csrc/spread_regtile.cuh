@@ -63,6 +63,7 @@ struct RegParams {
   int n1, n2;
   int m1, m2;  // runtime bin size (<= M1, M2 on tiny grids)
   int nb1;
+  int64_t cstride, gstride;  // per vector: M strengths, one fine grid
 };
 
 // Extended kernel values of one coordinate g (bin-relative, in [cell, cell+1)):
@@ -91,6 +92,8 @@ template <typename T, int W, int C>
 __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
   using G = RowSlide2D<T, W, C>;
   using CT = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
   struct __align__(16) Stage {
     T wy[G::S][G::WYS];
     T wx[G::S][G::WXS];
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
 template <typename T, int W, int C>
 cudaError_t spread_regtile2d_wc(const nufft_plan_s *p, const void *c) {
   using G = RowSlide2D<T, W, C>;
-  RegParams<T> a;
+  RegParams<T> a{};
   a.sub = p->subprob;
   a.nsub = (int)p->nsub;
   a.perm = p->perm;
@@ -250,8 +253,10 @@ cudaError_t spread_regtile2d_wc(const nufft_plan_s *p, const void *c) {
   a.m1 = p->m[0];
   a.m2 = p->m[1];
   a.nb1 = p->nb[0];
+  a.cstride = p->M;
+  a.gstride = grid_cells(p);
   const unsigned blocks = (unsigned)((p->nsub + G::WARPS - 1) / G::WARPS);
-  spread_regtile2d_kernel<T, W, C><<<blocks, 32 * G::WARPS, 0, p->stream>>>(a);
+  spread_regtile2d_kernel<T, W, C><<<dim3(blocks, p->nvec), 32 * G::WARPS, 0, p->stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -153,6 +153,7 @@ struct SIParams {
   int n1, n2, n3;
   int m1, m2, m3;
   int nb1, nb2;
+  int64_t cstride, gstride;  // per vector: M strengths, one fine grid
 };
 
 // Bin coordinates of a bin index (x fastest).
@@ -173,6 +174,8 @@ __device__ __forceinline__ void bin_coords(int bin, int nb1, int nb2, int &b1, i
 template <typename T, int DIM, int W>
 __global__ void spread_sm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T *tile = reinterpret_cast<T *>(smem_raw);  // interleaved (re, im)
   constexpr int PAD = (W + 1) / 2;
@@ -230,6 +233,8 @@ __global__ void spread_sm_kernel(SIParams<T> a) {
 template <typename T, int DIM, int W>
 __global__ void spread_gm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
   const Subproblem sp = a.sub[blockIdx.x];
   int b1, b2, b3;
   bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
@@ -264,6 +269,8 @@ __global__ void spread_gm_kernel(SIParams<T> a) {
 template <typename T, int DIM, int W>
 __global__ void interp_sm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   C *tile = reinterpret_cast<C *>(smem_raw);
   constexpr int PAD = (W + 1) / 2;
@@ -347,6 +354,8 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
 template <typename T, int DIM, int W>
 __global__ void interp_gm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
   const Subproblem sp = a.sub[blockIdx.x];
   int b1, b2, b3;
   bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
@@ -412,6 +421,8 @@ __device__ __forceinline__ void unpack_cell(int packed, int n1, int n2, int &l1,
 template <typename T, int DIM, int W>
 __global__ void spread_gmu_kernel(SIParams<T> a, int64_t M) {
   using C = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
   int c1, c2, c3;
@@ -443,6 +454,8 @@ __global__ void spread_gmu_kernel(SIParams<T> a, int64_t M) {
 template <typename T, int DIM, int W>
 __global__ void interp_gmu_kernel(SIParams<T> a, int64_t M) {
   using C = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= M) return;
   int c1, c2, c3;
@@ -487,7 +500,7 @@ __global__ void interp_gmu_kernel(SIParams<T> a, int64_t M) {
 
 template <typename T>
 SIParams<T> make_params(const nufft_plan_s *p) {
-  SIParams<T> a;
+  SIParams<T> a{};
   a.sub = p->subprob;
   a.perm = p->perm;
   a.g1 = static_cast<const T *>(p->gcoord[0]);
@@ -505,6 +518,8 @@ SIParams<T> make_params(const nufft_plan_s *p) {
   a.m3 = p->m[2];
   a.nb1 = p->nb[0];
   a.nb2 = p->nb[1];
+  a.cstride = p->M;
+  a.gstride = grid_cells(p);
   return a;
 }
 
@@ -530,18 +545,18 @@ cudaError_t spread_w(const nufft_plan_s *p, const void *c) {
   const unsigned blocks = (unsigned)p->nsub;
   if (p->method == NUFFT_METHOD_GM) {
     a.perm = p->bin_of;  // packed cells, caller's order
-    spread_gmu_kernel<T, DIM, W><<<(unsigned)((p->M + p->threads - 1) / p->threads), p->threads, 0,
+    spread_gmu_kernel<T, DIM, W><<<dim3((unsigned)((p->M + p->threads - 1) / p->threads), p->nvec), p->threads, 0,
                                    p->stream>>>(a, p->M);
     return cudaGetLastError();
   }
   if (p->method == NUFFT_METHOD_GM_SORT) {
-    spread_gm_kernel<T, DIM, W><<<blocks, p->threads, 0, p->stream>>>(a);
+    spread_gm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, 0, p->stream>>>(a);
     return cudaGetLastError();
   }
   const size_t smem = tile_cells(p) * 2 * sizeof(T);
   cudaError_t e = allow_smem(spread_sm_kernel<T, DIM, W>, smem);
   if (e != cudaSuccess) return e;
-  spread_sm_kernel<T, DIM, W><<<blocks, p->threads, smem, p->stream>>>(a);
+  spread_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -552,18 +567,18 @@ cudaError_t interp_w(const nufft_plan_s *p, void *c) {
   const unsigned blocks = (unsigned)p->nsub;
   if (p->method == NUFFT_METHOD_GM) {
     a.perm = p->bin_of;  // packed cells, caller's order
-    interp_gmu_kernel<T, DIM, W><<<(unsigned)((p->M + p->threads - 1) / p->threads), p->threads, 0,
+    interp_gmu_kernel<T, DIM, W><<<dim3((unsigned)((p->M + p->threads - 1) / p->threads), p->nvec), p->threads, 0,
                                    p->stream>>>(a, p->M);
     return cudaGetLastError();
   }
   if (p->method == NUFFT_METHOD_GM_SORT) {
-    interp_gm_kernel<T, DIM, W><<<blocks, p->threads, 0, p->stream>>>(a);
+    interp_gm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, 0, p->stream>>>(a);
     return cudaGetLastError();
   }
   const size_t smem = tile_cells(p) * 2 * sizeof(T);
   cudaError_t e = allow_smem(interp_sm_kernel<T, DIM, W>, smem);
   if (e != cudaSuccess) return e;
-  interp_sm_kernel<T, DIM, W><<<blocks, p->threads, smem, p->stream>>>(a);
+  interp_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
   return cudaGetLastError();
 }
 

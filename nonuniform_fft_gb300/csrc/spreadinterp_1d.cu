@@ -32,6 +32,7 @@ struct Params1D {
   CT *grid;
   T beta_e;
   int n1, m1;
+  int64_t cstride, gstride;  // per vector: M strengths, one fine grid
 };
 
 constexpr int kWarps1D = 4;
@@ -39,6 +40,8 @@ constexpr int kWarps1D = 4;
 template <typename T, int W>
 __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_kernel(Params1D<T> a) {
   using CT = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
   constexpr int PAD = (W + 1) / 2, HW = W / 2, S = 128;
   __shared__ T s_g[kWarps1D][S];
   __shared__ CT s_c[kWarps1D][S];
@@ -87,6 +90,8 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_kernel(Params1D<T>
 template <typename T, int W>
 __global__ void interp_sm1d_kernel(Params1D<T> a) {
   using CT = typename Cplx<T>::type;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
   constexpr int PAD = (W + 1) / 2;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   CT *tile = reinterpret_cast<CT *>(smem_raw);
@@ -116,7 +121,7 @@ __global__ void interp_sm1d_kernel(Params1D<T> a) {
 
 template <typename T>
 Params1D<T> params1d(const nufft_plan_s *p) {
-  Params1D<T> a;
+  Params1D<T> a{};
   a.sub = p->subprob;
   a.nsub = (int)p->nsub;
   a.perm = p->perm;
@@ -128,6 +133,8 @@ Params1D<T> params1d(const nufft_plan_s *p) {
   a.beta_e = (T)es_beta_e(p->beta, sizeof(T));
   a.n1 = (int)p->n[0];
   a.m1 = p->m[0];
+  a.cstride = p->M;
+  a.gstride = grid_cells(p);
   return a;
 }
 
@@ -135,7 +142,8 @@ template <typename T, int W>
 cudaError_t spread1d_w(const nufft_plan_s *p, const void *c) {
   Params1D<T> a = params1d<T>(p);
   a.c_in = static_cast<const typename Cplx<T>::type *>(c);
-  spread_reg1d_kernel<T, W><<<(unsigned)((p->nsub + kWarps1D - 1) / kWarps1D), 32 * kWarps1D, 0,
+  spread_reg1d_kernel<T, W><<<dim3((unsigned)((p->nsub + kWarps1D - 1) / kWarps1D), p->nvec),
+                              32 * kWarps1D, 0,
                               p->stream>>>(a);
   return cudaGetLastError();
 }
@@ -147,7 +155,7 @@ cudaError_t interp1d_w(const nufft_plan_s *p, void *c) {
   const size_t smem = (size_t)(p->m[0] + 2 * ((W + 1) / 2)) * 2 * sizeof(T);
   cudaError_t e = allow_smem(interp_sm1d_kernel<T, W>, smem);
   if (e != cudaSuccess) return e;
-  interp_sm1d_kernel<T, W><<<(unsigned)p->nsub, p->threads, smem, p->stream>>>(a);
+  interp_sm1d_kernel<T, W><<<dim3((unsigned)p->nsub, p->nvec), p->threads, smem, p->stream>>>(a);
   return cudaGetLastError();
 }
 

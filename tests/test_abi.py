@@ -92,11 +92,12 @@ def test_null_plan_calls(lib):
     assert lib.nufft_set_opt(None, b"msub", 64.0) == nf.ERR_BAD_ARG
     assert lib.nufft_setpts(None, 10, None, None, None) == nf.ERR_BAD_ARG
     assert lib.nufft_execute(None, None, None) == nf.ERR_BAD_ARG
+    assert lib.nufft_execute_batch(None, 1, None, None) == nf.ERR_BAD_ARG
     assert lib.nufft_destroy(None) == nf.OK
     buf = (ctypes.c_double * 6)()
     assert lib.nufft_get_timings(None, buf, 6) == nf.ERR_BAD_ARG
-    ibuf = (ctypes.c_int64 * 12)()
-    assert lib.nufft_get_info(None, ibuf, 12) == nf.ERR_BAD_ARG
+    ibuf = (ctypes.c_int64 * 13)()
+    assert lib.nufft_get_info(None, ibuf, 13) == nf.ERR_BAD_ARG
     assert lib.nufft_get_sort(None, None, None, None, None) == nf.ERR_BAD_ARG
     assert lib.nufft_makeplan(1, 2, (ctypes.c_int64 * 2)(8, 8), -1, 1e-6, 0, None, None) == nf.ERR_BAD_ARG
 
