@@ -30,8 +30,19 @@ Readings of points the paper leaves open (each also listed in the design notes):
 * w = ceil(log10(1/eps)) + 1 (eq. (6)); a tolerance within 1e-9 (in log10) of a
   power of ten counts as that power, so decimal literals such as 1e-6 give the
   widths [finufft#809] lists (1e-3 -> 4, 1e-6 -> 7, 1e-9 -> 10, 1e-12 -> 13).
-* Fine grid n_i: the smallest 2^a 3^b 5^c that is >= max(2 N_i, 2 w)
-  (Sec. II, text after eq. (6), with sigma = 2).
+* Fine grid n_i: the smallest 2^a 3^b 5^c that is >= max(sigma N_i, 2 w)
+  (Sec. II, text after eq. (6)); sigma = 2 unless a smaller upsampling factor
+  is asked for.
+* sigma < 2 ([cuFINUFFT] Sec. I-B limitation 3 and Sec. V name it as future
+  work, citing the ES-kernel paper, but give no width rule for it): eq. (6)
+  with its sigma dependence taken from the ES kernel's error law, which decays
+  like exp(-pi w sqrt(1 - 1/sigma)).  Relative to sigma = 2 that stretches the
+  digit count by 1/sqrt(2 (1 - 1/sigma)), and beta scales with
+  (1 - 1/(2 sigma)) as in that paper:
+      w = ceil(log10(1/eps) / sqrt(2 (1 - 1/sigma))) + 1,
+      beta = 2.30 w (4/3) (1 - 1/(2 sigma)),
+  which is eq. (6) itself at sigma = 2 (used verbatim there).  Accepted:
+  1 < sigma <= 2.
 * Fine-grid node l sits at l h (eq. (7)); a coordinate is reduced to one period
   [0, 2 pi) before use, so any finite coordinate is valid.
 * A point touches the w nodes with kernel argument z in [-1, 1).
@@ -131,21 +142,31 @@ def _coords(pts):
 # Parameters ([cuFINUFFT] Sec. II eq. (6) and the text after it)
 # --------------------------------------------------------------------------
 
-def es_params(eps: float) -> tuple[int, float]:
-    """Kernel width w and ES shape beta for tolerance eps, [cuFINUFFT] eq. (6)."""
+def _snap(v: float) -> float:
+    """A value within 1e-9 (relative) of an integer counts as that integer, so
+    decimal inputs do not flip a ceiling on rounding noise."""
+    r = round(v)
+    return float(r) if abs(v - r) <= 1e-9 * max(1.0, abs(v)) else v
+
+
+def es_params(eps: float, sigma: float = 2.0) -> tuple[int, float]:
+    """Kernel width w and ES shape beta for tolerance eps, [cuFINUFFT] eq. (6)
+    at sigma = 2; the sigma < 2 reading in the module notes otherwise."""
     if not eps > 0:
         raise ValueError("eps must be > 0")
-    L = -math.log10(eps)
-    r = round(L)
-    if abs(L - r) < 1e-9:
-        L = float(r)
-    w = int(math.ceil(L)) + 1
-    return w, 2.30 * w
+    if not 1.0 < sigma <= 2.0:
+        raise ValueError("sigma must be in (1, 2]")
+    L = _snap(-math.log10(eps))
+    if sigma == 2.0:
+        w = int(math.ceil(L)) + 1
+        return w, 2.30 * w
+    w = int(math.ceil(_snap(L / math.sqrt(2.0 * (1.0 - 1.0 / sigma))))) + 1
+    return w, 2.30 * w * (4.0 / 3.0) * (1.0 - 0.5 / sigma)
 
 
-def fine_grid_size(N: int, w: int) -> int:
-    """Smallest 2^a 3^b 5^c >= max(2 N, 2 w) (sigma = 2)."""
-    target = max(2 * N, 2 * w)
+def fine_grid_size(N: int, w: int, sigma: float = 2.0) -> int:
+    """Smallest 2^a 3^b 5^c >= max(sigma N, 2 w)."""
+    target = max(int(math.ceil(_snap(sigma * N))), 2 * w)
     n = target
     while True:
         m = n
@@ -270,9 +291,9 @@ def direct_type2(pts, f, N, iflag: int, targets=None) -> np.ndarray:
 # O2: three-step NUFFT ([cuFINUFFT] Sec. II)
 # --------------------------------------------------------------------------
 
-def plan_params(N, eps: float):
-    w, beta = es_params(eps)
-    n = [fine_grid_size(Ni, w) for Ni in N]
+def plan_params(N, eps: float, sigma: float = 2.0):
+    w, beta = es_params(eps, sigma)
+    n = [fine_grid_size(Ni, w, sigma) for Ni in N]
     return w, beta, n
 
 
@@ -318,11 +339,11 @@ def _outer(ps):
     return out
 
 
-def nufft_type1(pts, c, N, eps: float, iflag: int) -> np.ndarray:
+def nufft_type1(pts, c, N, eps: float, iflag: int, sigma: float = 2.0) -> np.ndarray:
     """O2 type 1: spread (eq. (7)), FFT (eq. (9)), truncate + correct (eq. (10)).
     Returns f shaped (N3,) N2, N1."""
     N = list(N)
-    w, beta, n = plan_params(N, eps)
+    w, beta, n = plan_params(N, eps, sigma)
     b = spread(pts, c, n, w, beta)
     bhat = _fft(b, iflag)
     idx = [_fine_index(Ni, ni) for Ni, ni in zip(N, n)]
@@ -331,11 +352,11 @@ def nufft_type1(pts, c, N, eps: float, iflag: int) -> np.ndarray:
     return p * sub
 
 
-def nufft_type2(pts, f, N, eps: float, iflag: int) -> np.ndarray:
+def nufft_type2(pts, f, N, eps: float, iflag: int, sigma: float = 2.0) -> np.ndarray:
     """O2 type 2: pre-correct + zero-pad (eq. (11)), FFT (eq. (12)),
     interpolate (Sec. II-B c).  f shaped (N3,) N2, N1 or flat."""
     N = list(N)
-    w, beta, n = plan_params(N, eps)
+    w, beta, n = plan_params(N, eps, sigma)
     f = _c128(f).reshape(tuple(reversed(N)))
     p = _outer([correction_factors(Ni, ni, w, beta) for Ni, ni in zip(N, n)])
     bhat = np.zeros(tuple(reversed(n)), dtype=np.complex128)

@@ -63,7 +63,8 @@ def _mut_correction_inverted(monkeypatch):
 
 def _mut_width_minus_one(monkeypatch):
     orig = oracle.es_params
-    monkeypatch.setattr(oracle, "es_params", lambda eps: (orig(eps)[0] - 1, 2.30 * (orig(eps)[0] - 1)))
+    monkeypatch.setattr(oracle, "es_params",
+                        lambda eps, sigma=2.0: (orig(eps)[0] - 1, 2.30 * (orig(eps)[0] - 1)))
 
 
 def _mut_transposed_modes(monkeypatch):
@@ -80,6 +81,44 @@ def _mut_mode_offset(monkeypatch):
 def _mut_phihat_scaled(monkeypatch):
     orig = oracle.phihat
     monkeypatch.setattr(oracle, "phihat", lambda xi, beta, q=200: orig(np.asarray(xi) * 1.05, beta, q))
+
+
+def _sigma_sweep_ok(eps=1e-6, N=(48, 40), M=1500, sigma=1.25):
+    rng = np.random.default_rng(3)
+    pts = [rng.uniform(-np.pi, np.pi, M) for _ in N]
+    c = rng.standard_normal(M) + 1j * rng.standard_normal(M)
+    e = oracle.rel_l2(oracle.nufft_type1(pts, c, N, eps, -1, sigma),
+                      oracle.direct_type1(pts, c, N, -1))
+    return eps / 8 <= e <= 3 * eps
+
+
+def _mut_sigma_beta_of_two(monkeypatch):
+    orig = oracle.es_params
+    # the sigma < 2 width with the sigma = 2 shape beta = 2.30 w
+    monkeypatch.setattr(oracle, "es_params",
+                        lambda eps, sigma=2.0: (orig(eps, sigma)[0], 2.30 * orig(eps, sigma)[0]))
+
+
+def _mut_sigma_grid_of_two(monkeypatch):
+    orig = oracle.fine_grid_size
+    # the sigma < 2 kernel on the sigma = 2 grid
+    monkeypatch.setattr(oracle, "fine_grid_size", lambda N, w, sigma=2.0: orig(N, w))
+
+
+def _mut_sigma_width_of_two(monkeypatch):
+    orig = oracle.es_params
+    # eq. (6) width for every sigma, with the sigma < 2 beta scaling
+    monkeypatch.setattr(oracle, "es_params",
+                        lambda eps, sigma=2.0: (orig(eps)[0],
+                                                orig(eps, sigma)[1] / orig(eps, sigma)[0] * orig(eps)[0]))
+
+
+@pytest.mark.parametrize("mutate", [_mut_sigma_beta_of_two, _mut_sigma_grid_of_two,
+                                    _mut_sigma_width_of_two])
+def test_planted_sigma_mistake_is_caught(monkeypatch, mutate):
+    assert _sigma_sweep_ok()
+    mutate(monkeypatch)
+    assert not _sigma_sweep_ok()
 
 
 @pytest.mark.parametrize("mutate", [_mut_fft_sign, _mut_no_correction, _mut_correction_inverted,

@@ -220,6 +220,59 @@ def test_nufft_error_close_to_eps(dim, N, M, eps):
             assert e1 >= eps / 4 and e2 >= eps / 4
 
 
+def test_sigma_rule_is_eq6_at_two():
+    """The sigma < 2 reading reduces to eq. (6) itself at sigma = 2."""
+    for tol in (0.5, 1e-2, 1e-3, 5e-4, 1e-5, 1e-6, 1e-9, 1e-12, 1e-15):
+        assert oracle.es_params(tol, 2.0) == oracle.es_params(tol)
+        for N in (1, 7, 64, 1000):
+            w = oracle.es_params(tol)[0]
+            assert oracle.fine_grid_size(N, w, 2.0) == oracle.fine_grid_size(N, w)
+
+
+def test_sigma_rule_hand_values():
+    """Worked by hand: sigma = 1.25, eps = 1e-6: 6 / sqrt(2 * 0.2) = 9.49 ->
+    w = 11, beta = 2.30 * 11 * (4/3) * 0.6 = 20.24; sigma = 1.5, eps = 1e-3:
+    3 / sqrt(2/3) = 3.67 -> w = 5, beta = 2.30 * 5 * (4/3) * (2/3) = 10.22;
+    grids: 1.25 * 100 = 125 = 5^3; 1.5 * 64 = 96 = 2^5 3; 1.5 * 30 = 45 but
+    2 w = 22 < 45 -> 45 = 3^2 5; 1.25 * 10 = 12.5 -> 13 -> 15 = 3 5."""
+    w, beta = oracle.es_params(1e-6, 1.25)
+    assert w == 11 and abs(beta - 20.24) < 1e-12
+    w, beta = oracle.es_params(1e-3, 1.5)
+    assert w == 5 and abs(beta - 2.30 * 5 * 8 / 9) < 1e-12
+    assert oracle.fine_grid_size(100, 11, 1.25) == 125
+    assert oracle.fine_grid_size(64, 5, 1.5) == 96
+    assert oracle.fine_grid_size(30, 11, 1.5) == 45
+    assert oracle.fine_grid_size(10, 4, 1.25) == 15
+    with pytest.raises(ValueError):
+        oracle.es_params(1e-6, 1.0)
+    with pytest.raises(ValueError):
+        oracle.es_params(1e-6, 2.5)
+
+
+@pytest.mark.parametrize("dim,N,M", [(1, (200,), 3000), (2, (48, 40), 3000), (3, (24, 20, 28), 2000)])
+@pytest.mark.parametrize("sigma", [1.25, 1.5])
+@pytest.mark.parametrize("eps", [1e-2, 1e-3, 1e-6, 1e-9])
+def test_nufft_error_close_to_eps_sigma(dim, N, M, sigma, eps):
+    """sigma < 2 ([cuFINUFFT] Sec. I-B limitation 3): with the stretched
+    eq. (6) the error against the direct sums stays 'close to eps', here
+    within [eps/8, 3 eps] for both types and signs, on a grid smaller than
+    the sigma = 2 one.  A grid or beta taken from sigma = 2 by mistake makes
+    the error orders of magnitude smaller than eps; a beta for the wrong
+    sigma, orders larger."""
+    rng = np.random.default_rng(9)
+    pts = [rng.uniform(-np.pi, np.pi, M) for _ in range(dim)]
+    c = rng.standard_normal(M) + 1j * rng.standard_normal(M)
+    f = rng.standard_normal(int(np.prod(N))) + 1j * rng.standard_normal(int(np.prod(N)))
+    w, _, n = oracle.plan_params(N, eps, sigma)
+    assert any(ni < 2 * Ni for ni, Ni in zip(n, N))
+    for iflag in (-1, 1):
+        e1 = oracle.rel_l2(oracle.nufft_type1(pts, c, N, eps, iflag, sigma),
+                           oracle.direct_type1(pts, c, N, iflag))
+        e2 = oracle.rel_l2(oracle.nufft_type2(pts, f, N, eps, iflag, sigma),
+                           oracle.direct_type2(pts, f, N, iflag))
+        assert eps / 8 <= e1 <= 3 * eps and eps / 8 <= e2 <= 3 * eps, (e1 / eps, e2 / eps)
+
+
 @pytest.mark.parametrize("N", [(20,), (16, 12), (8, 10, 6)])
 def test_nufft_single_point(N):
     """c = 1 at x0: f_k ~ exp(-i k.x0) (|f_k| = 1) within eps; x0 anywhere,
