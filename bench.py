@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="points per transform in the CPU baseline sample (0: auto)")
+    ap.add_argument("--sigma", type=float, default=2.0,
+                    help="upsampling factor in (1, 2] (nufft_makeplan_upsampled when < 2)")
     ap.add_argument("--batch", type=int, default=1,
                     help="strength vectors per transform (nufft_execute_batch); 1: nufft_execute")
     ap.add_argument("--opt", action="append", default=[], metavar="KEY=VALUE",
@@ -180,16 +182,16 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def cpu_sample_points(wl: W.Workload, budget_cells: float = 1.2e8) -> int:
+def cpu_sample_points(wl: W.Workload, budget_cells: float = 1.2e8, sigma: float = 2.0) -> int:
     """Points in a CPU-oracle sample: about budget_cells kernel-weighted grid
     updates per transform (w^d per point), so that every workload's sample
     takes seconds, not minutes."""
     import oracle
-    w = oracle.es_params(wl.eps)[0]
+    w = oracle.es_params(wl.eps, sigma)[0]
     return int(min(wl.M, max(20000, budget_cells / w ** wl.dim)))
 
 
-def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1) -> dict:
+def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1, sigma: float = 2.0) -> dict:
     """Time the oracle's three-step NUFFT (type 1, plus type 2 when the
     workload has it) on the first sample_M points of the workload; returns
     points/s over `steps` repeats."""
@@ -200,16 +202,16 @@ def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1) -> dict:
     oracle.build()
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1])
+        oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1], sigma)
         if 2 in wl.types:
-            oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2])
+            oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2], sigma)
     dt = time.perf_counter() - t0
     per_step = sample_M * len(wl.types)
     types = " + ".join(f"type {t}" for t in wl.types)
     return {"value": per_step * steps / dt, "unit": "NU points/s", "cores": 1,
             "kind": "oracle", "seconds": dt,
             "sample": f"{sample_M} of {wl.M} points of {wl.name}, full {'x'.join(map(str, wl.N))} "
-                      f"modes, {types}, x{steps}; double precision, one thread"}
+                      f"modes, {types}, x{steps}; sigma {sigma:g}; double precision, one thread"}
 
 
 def run_reference(args, wl):
@@ -218,18 +220,18 @@ def run_reference(args, wl):
         return 0
     # bounded: about a minute of CPU work for the whole --steps + --warmup run
     per_step = args.cpu_sample or max(
-        5000, cpu_sample_points(wl, 1.2e8 / max(1, (args.steps + args.warmup) / 2)))
+        5000, cpu_sample_points(wl, 1.2e8 / max(1, (args.steps + args.warmup) / 2), args.sigma))
     per_step = min(per_step, wl.M)
     if args.warmup:
-        cpu_oracle_run(wl, min(per_step, 20000), 1)
-    r = cpu_oracle_run(wl, per_step, args.steps)
+        cpu_oracle_run(wl, min(per_step, 20000), 1, args.sigma)
+    r = cpu_oracle_run(wl, per_step, args.steps, args.sigma)
     line = {
         "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "NU points/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * r["seconds"] / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "N": list(wl.N), "M": wl.M, "eps": wl.eps,
-                   "sample_points_per_transform": per_step},
+                   "sigma": args.sigma, "sample_points_per_transform": per_step},
         "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": r["value"], "unit": "NU points/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -276,11 +278,13 @@ def run_ours(args, wl):
     del pts
 
     opts = plan_opts(args)
-    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream, **opts)
+    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
+                 **opts)
     p1.setpts(*xs)
     p2 = None
     if 2 in wl.types:
-        p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream, **opts)
+        p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
+                     **opts)
         p2.setpts(*xs)
     info = p1.info()
     n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
@@ -412,7 +416,8 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_run(wl, args.cpu_sample or cpu_sample_points(wl), 1)
+        cpu = cpu_oracle_run(wl, args.cpu_sample or cpu_sample_points(wl, sigma=args.sigma), 1,
+                             args.sigma)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:
@@ -423,7 +428,8 @@ def run_ours(args, wl):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": wl.name, "dim": wl.dim, "N": list(wl.N), "M": wl.M,
-                       "eps": wl.eps, "w": info["w"], "fine_grid": n, "dist": wl.dist,
+                       "eps": wl.eps, "sigma": args.sigma, "w": info["w"], "fine_grid": n,
+                       "dist": wl.dist,
                        "types": " + ".join(f"type {t} (iflag {wl.iflag[t]:+d})" for t in wl.types)
                                 + " per step",
                        "points_per_step_per_gpu": pts_per_step,

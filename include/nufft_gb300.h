@@ -115,6 +115,24 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
                    int dtype, void *cuda_stream, nufft_plan_t *out);
 
 /*
+ * nufft_makeplan with an upsampling factor sigma in (1, 2] instead of the
+ * paper's fixed sigma = 2 (Sec. I-B, limitation 3, names smaller sigma as a way
+ * to cut memory and run time; Sec. II gives the rule only for sigma = 2).
+ * Rule used (eq. (6) at sigma = 2, and otherwise eq. (6) with the sigma
+ * dependence of the ES kernel's error, which decays like
+ * exp(-pi w sqrt(1 - 1/sigma))):
+ *   w    = ceil(log10(1/eps) / sqrt(2 (1 - 1/sigma))) + 1,
+ *   beta = 2.30 w (4/3) (1 - 1/(2 sigma)),
+ *   n_i  = smallest 2^a 3^b 5^c >= max(sigma N_i, 2 w).
+ * Products within 1e-9 of an integer count as that integer before a ceiling.
+ * Smaller sigma means a smaller fine grid and FFT but a wider kernel.
+ * Errors: as nufft_makeplan; BAD_ARG also for sigma outside (1, 2] or NaN;
+ * BAD_EPS when the width comes out above 16.
+ */
+int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int iflag, double eps,
+                             int dtype, double sigma, void *cuda_stream, nufft_plan_t *out);
+
+/*
  * Set a tuning option; takes effect at the next setpts.  Keys:
  *   "method"   NUFFT_METHOD_* (type 1 spreading; type 2 always uses the
  *              tiled shared-memory interpolator unless "method" is GM_SORT).

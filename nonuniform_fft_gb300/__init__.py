@@ -55,6 +55,8 @@ def load_library(path: str | None = None):
     lib = ctypes.CDLL(path)
     P, I, I64, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
     lib.nufft_makeplan.argtypes = [I, I, ctypes.POINTER(I64), I, D, I, P, ctypes.POINTER(P)]
+    lib.nufft_makeplan_upsampled.argtypes = [I, I, ctypes.POINTER(I64), I, D, I, D, P,
+                                             ctypes.POINTER(P)]
     lib.nufft_set_opt.argtypes = [P, ctypes.c_char_p, D]
     lib.nufft_setpts.argtypes = [P, I64, P, P, P]
     lib.nufft_execute.argtypes = [P, P, P]
@@ -65,7 +67,7 @@ def load_library(path: str | None = None):
     lib.nufft_get_sort.argtypes = [P, P, P, P, P]
     lib.nufft_strerror.argtypes = [I]
     lib.nufft_strerror.restype = ctypes.c_char_p
-    for name in ("nufft_makeplan", "nufft_set_opt", "nufft_setpts", "nufft_execute",
+    for name in ("nufft_makeplan", "nufft_makeplan_upsampled", "nufft_set_opt", "nufft_setpts", "nufft_execute",
                  "nufft_execute_batch", "nufft_destroy", "nufft_get_timings", "nufft_get_info",
                  "nufft_get_sort"):
         getattr(lib, name).restype = I
@@ -110,17 +112,24 @@ def strerror(code: int) -> str:
 
 
 def makeplan(type: int, n_modes, iflag: int, eps: float, dtype: str = "complex64",
-             stream: int | None = None) -> int:
-    """nufft_makeplan: returns an opaque plan handle.  dtype 'complex64' or
-    'complex128'; stream a cudaStream_t value (default: torch's current)."""
+             stream: int | None = None, sigma: float = 2.0) -> int:
+    """nufft_makeplan (sigma = 2) or nufft_makeplan_upsampled: returns an
+    opaque plan handle.  dtype 'complex64' or 'complex128'; stream a
+    cudaStream_t value (default: torch's current)."""
     lib = load_library()
     dims = list(n_modes)
     arr = (ctypes.c_int64 * len(dims))(*dims)
     code_dtype = {"complex64": 0, "complex128": 1}[str(dtype).replace("torch.", "")]
     out = ctypes.c_void_p()
     s = _current_stream() if stream is None else stream
-    _check(lib.nufft_makeplan(int(type), len(dims), arr, int(iflag), float(eps), code_dtype,
-                              ctypes.c_void_p(s) if s else None, ctypes.byref(out)), "makeplan")
+    sp = ctypes.c_void_p(s) if s else None
+    if float(sigma) == 2.0:
+        rc = lib.nufft_makeplan(int(type), len(dims), arr, int(iflag), float(eps), code_dtype, sp,
+                                ctypes.byref(out))
+    else:
+        rc = lib.nufft_makeplan_upsampled(int(type), len(dims), arr, int(iflag), float(eps),
+                                          code_dtype, float(sigma), sp, ctypes.byref(out))
+    _check(rc, "makeplan")
     return out.value
 
 
@@ -175,11 +184,12 @@ class Plan:
     """Owning wrapper: Plan(type, n_modes, iflag, eps, dtype) ... close()."""
 
     def __init__(self, type: int, n_modes, iflag: int, eps: float, dtype: str = "complex64",
-                 stream: int | None = None, **opts):
+                 stream: int | None = None, sigma: float = 2.0, **opts):
         self.type = type
         self.n_modes = tuple(int(n) for n in n_modes)
         self.dtype = dtype
-        self.handle = makeplan(type, self.n_modes, iflag, eps, dtype, stream)
+        self.handle = None
+        self.handle = makeplan(type, self.n_modes, iflag, eps, dtype, stream, sigma)
         for k, v in opts.items():
             set_opt(self.handle, k, v)
         self.M = 0

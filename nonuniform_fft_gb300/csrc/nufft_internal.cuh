@@ -35,6 +35,7 @@ struct nufft_plan_s {
   int iflag = -1;
   int dtype = 0;  // 0 complex64, 1 complex128
   double eps = 0;
+  double sigma = 2.0;  // upsampling factor
   int w = 0;
   double beta = 0;
   int64_t N[3] = {1, 1, 1};

@@ -23,14 +23,29 @@ constexpr double kPi = 3.14159265358979323846;
 
 // ---------------------------------------------------------------- parameters
 
-// Kernel width from eq. (6): w = ceil(log10(1/eps)) + 1.  A tolerance whose
-// log10 is within 1e-9 of an integer counts as that power of ten, so that
-// decimal literals such as 1e-6 give w = 7.
-int width_for(double eps) {
-  double L = -std::log10(eps);
-  const double r = std::nearbyint(L);
-  if (std::fabs(L - r) < 1e-9) L = r;
-  return (int)std::ceil(L) + 1;
+// A value within 1e-9 (relative) of an integer is taken as that integer, so
+// decimal tolerances and factors do not flip a ceiling on rounding noise
+// (1e-6 gives log10 = 6 exactly, hence w = 7).
+double snap_int(double v) {
+  const double r = std::nearbyint(v);
+  return std::fabs(v - r) <= 1e-9 * std::max(1.0, std::fabs(v)) ? r : v;
+}
+
+// Kernel width: eq. (6), w = ceil(log10(1/eps)) + 1, at sigma = 2.  For
+// sigma < 2 the digit count is stretched by 1 / sqrt(2 (1 - 1/sigma)), the
+// ratio of the ES kernel's error exponents pi w sqrt(1 - 1/sigma) at sigma = 2
+// and at sigma (the paper fixes sigma = 2 and gives no rule for other values).
+int width_for(double eps, double sigma) {
+  const double L = snap_int(-std::log10(eps));
+  if (sigma == 2.0) return (int)std::ceil(L) + 1;
+  return (int)std::ceil(snap_int(L / std::sqrt(2.0 * (1.0 - 1.0 / sigma)))) + 1;
+}
+
+// Kernel shape: eq. (6), beta = 2.30 w, at sigma = 2; for sigma < 2 scaled by
+// (1 - 1/(2 sigma)) / (3/4), the ES kernel's optimal-shape dependence.
+double beta_for(int w, double sigma) {
+  if (sigma == 2.0) return 2.30 * w;
+  return 2.30 * w * (4.0 / 3.0) * (1.0 - 0.5 / sigma);
 }
 
 // Smallest 2^a 3^b 5^c >= v.
@@ -261,14 +276,19 @@ const char *nufft_strerror(int code) {
 
 int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double eps, int dtype,
                    void *cuda_stream, nufft_plan_t *out) {
+  return nufft_makeplan_upsampled(type, dim, n_modes, iflag, eps, dtype, 2.0, cuda_stream, out);
+}
+
+int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int iflag, double eps,
+                             int dtype, double sigma, void *cuda_stream, nufft_plan_t *out) {
   if (out) *out = nullptr;
   if (!out || !n_modes || (type != 1 && type != 2) || dim < 1 || dim > 3 ||
-      (dtype != 0 && dtype != 1))
+      (dtype != 0 && dtype != 1) || !(sigma > 1.0 && sigma <= 2.0))
     return NUFFT_ERR_BAD_ARG;
   for (int d = 0; d < dim; d++)
     if (n_modes[d] < 1) return NUFFT_ERR_BAD_ARG;
   if (!(eps > 0) || !std::isfinite(eps)) return NUFFT_ERR_BAD_EPS;
-  const int w = width_for(eps);
+  const int w = width_for(eps, sigma);
   if (w < nufft::kMinWidth || w > nufft::kMaxWidth) return NUFFT_ERR_BAD_EPS;
 
   nufft_plan_s *p = new (std::nothrow) nufft_plan_s();
@@ -279,7 +299,8 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
   p->dtype = dtype;
   p->eps = eps;
   p->w = w;
-  p->beta = 2.30 * w;
+  p->beta = beta_for(w, sigma);
+  p->sigma = sigma;
   int64_t cells = 1, modes = 1;
   for (int d = 0; d < dim; d++) {
     p->N[d] = n_modes[d];
@@ -287,7 +308,9 @@ int nufft_makeplan(int type, int dim, const int64_t *n_modes, int iflag, double 
       delete p;
       return NUFFT_ERR_TOO_LARGE;
     }
-    p->n[d] = next_smooth(std::max<int64_t>(2 * p->N[d], 2 * (int64_t)w));
+    // fine grid: smallest 2^a 3^b 5^c >= max(sigma N_i, 2 w) (Sec. II, after eq. (6))
+    const int64_t sn = (int64_t)std::ceil(snap_int(sigma * (double)p->N[d]));
+    p->n[d] = next_smooth(std::max<int64_t>(sn, 2 * (int64_t)w));
     cells *= p->n[d];
     modes *= p->N[d];
   }

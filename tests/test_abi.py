@@ -88,6 +88,27 @@ def test_makeplan_rejects_bad_arguments(lib, args, code):
     assert plan is None
 
 
+@pytest.mark.parametrize("sigma,code", [(1.0, nf.ERR_BAD_ARG), (0.5, nf.ERR_BAD_ARG),
+                                        (2.5, nf.ERR_BAD_ARG), (float("nan"), nf.ERR_BAD_ARG),
+                                        (-1.5, nf.ERR_BAD_ARG)])
+def test_makeplan_upsampled_rejects_bad_sigma(lib, sigma, code):
+    arr = (ctypes.c_int64 * 2)(8, 8)
+    out = ctypes.c_void_p(1234)
+    assert lib.nufft_makeplan_upsampled(1, 2, arr, -1, 1e-6, 0, sigma, None, ctypes.byref(out)) == code
+    assert out.value is None
+
+
+def test_makeplan_upsampled_width_limit(lib):
+    """sigma = 1.25 stretches eq. (6): eps = 1e-10 needs w = ceil(10 / sqrt(0.4)) + 1
+    = 17 > 16, rejected before any device work; at sigma = 2 eps = 1e-10 is fine
+    in principle (w = 11) but needs a GPU, so only the rejection is checked."""
+    arr = (ctypes.c_int64 * 2)(8, 8)
+    out = ctypes.c_void_p(1234)
+    assert lib.nufft_makeplan_upsampled(1, 2, arr, -1, 1e-10, 1, 1.25, None,
+                                        ctypes.byref(out)) == nf.ERR_BAD_EPS
+    assert out.value is None
+
+
 def test_null_plan_calls(lib):
     assert lib.nufft_set_opt(None, b"msub", 64.0) == nf.ERR_BAD_ARG
     assert lib.nufft_setpts(None, 10, None, None, None) == nf.ERR_BAD_ARG

@@ -345,3 +345,27 @@ def test_plan_reuse_new_strengths_and_points():
                 plan.execute(torch.from_numpy(c).to(DEV), f)
                 ref = oracle.nufft_type1(pts, c, N, 1e-6, -1)
                 assert oracle.rel_l2(f.cpu().numpy(), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("dim,N", [(1, (700,)), (2, (60, 44)), (3, (16, 12, 20))])
+@pytest.mark.parametrize("eps", [1e-14, 1e-15])
+@pytest.mark.parametrize("ttype", [1, 2])
+def test_widest_kernels(dim, N, eps, ttype):
+    """w = 15 and 16 (eq. (6) at eps = 1e-14, 1e-15), the widest the library
+    accepts, in double precision: against the oracle NUFFT at 1e-12 and the
+    direct sums at the double-precision floor (1e-12)."""
+    rng = np.random.default_rng(23)
+    M = 6000
+    pts = _pts(dim, M, "uniform", rng, "f64")
+    iflag = 1 if ttype == 1 else -1
+    if ttype == 1:
+        c = _cplx(M, rng, "f64")
+        f = gpu_transform(1, pts, c, N, eps, iflag, "f64")
+        assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, iflag)) <= 1e-12
+        assert oracle.rel_l2(f, oracle.direct_type1(pts, c, N, iflag)) <= 1e-12
+    else:
+        fk = _cplx(int(np.prod(N)), rng, "f64")
+        c = gpu_transform(2, pts, fk, N, eps, iflag, "f64")
+        assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, eps, iflag)) <= 1e-12
+        tg = np.arange(0, M, 13)
+        assert oracle.rel_l2(c[tg], oracle.direct_type2(pts, fk, N, iflag, targets=tg)) <= 1e-12
