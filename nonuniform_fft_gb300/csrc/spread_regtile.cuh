@@ -37,16 +37,50 @@ struct RowSlide2D {
   static constexpr int HW = W / 2;          // floor(w/2)
   static constexpr int WX = W + 1;          // extended window
   static constexpr int VEC = 16 / (int)sizeof(T);
-  static constexpr int WXP = (WX + VEC - 1) / VEC * VEC;
-  // row strides of the staging buffer, chosen against bank conflicts between
-  // lanes reading different points
-  static constexpr int WYS = (WXP * (int)sizeof(T)) % 128 == 0 || (WXP * (int)sizeof(T)) % 64 == 0
-                                 ? WXP + VEC : WXP;
+  // staged y weights: WX values, then the point's cell offset xb in slot WX
+  static constexpr int WXP = (WX + 1 + VEC - 1) / VEC * VEC;
+  // row stride of the y weights: an odd number of 16-byte units, so that the
+  // 8 lanes of a quarter warp moving 16 bytes each hit 8 different bank quads
+  static constexpr int WYS = (WXP / VEC) % 2 == 0 ? WXP + VEC : WXP;
   static constexpr int WXE = W + 2 * C - 1;  // x weights seen by C columns, zero-padded
-  static constexpr int WXS = WXE | 1;        // odd stride
+  static constexpr int WCS = WXE | 1;        // odd row stride of the c * x-weight products
   static constexpr int M1 = 32 * C - 2 * PAD;  // bin width: C tile columns per lane
-  static constexpr int S = sizeof(T) == 4 ? 64 : 32;  // staged points per batch
+  // staged points per batch (measured on the 2D bench workload: 64 beats 96
+  // for one column per lane although 96 holds a whole bin row; the wider
+  // rows of two columns per lane prefer 96)
+  static constexpr int S = sizeof(T) == 4 ? (C == 2 && W <= 7 ? 96 : 64) : 32;
   static constexpr int WARPS = 4;
+};
+
+// 16-byte vector of T.
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  using type = float4;
+  static __device__ __forceinline__ void put(float *dst, const float *v) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+  static __device__ __forceinline__ void get(const float *src, float *v) {
+    const float4 t = *reinterpret_cast<const float4 *>(src);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  }
+};
+template <> struct Vec16<double> {
+  using type = double2;
+  static __device__ __forceinline__ void put(double *dst, const double *v) {
+    *reinterpret_cast<double2 *>(dst) = make_double2(v[0], v[1]);
+  }
+  static __device__ __forceinline__ void get(const double *src, double *v) {
+    const double2 t = *reinterpret_cast<const double2 *>(src);
+    v[0] = t.x; v[1] = t.y;
+  }
+};
+
+// Per-warp staging buffer of one batch of points.
+template <typename T, int W, int C>
+struct __align__(16) RegStage {
+  using G = RowSlide2D<T, W, C>;
+  T wy[G::S][G::WYS];                          // y weights; [WX]: cell offset xb
+  typename Cplx<T>::type cwx[G::S][G::WCS];    // c_j times the x weights
 };
 
 template <typename T>
@@ -94,15 +128,10 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
   using CT = typename Cplx<T>::type;
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
-  struct __align__(16) Stage {
-    T wy[G::S][G::WYS];
-    T wx[G::S][G::WXS];
-    CT c[G::S];
-    int xb[G::S];
-  };
-  __shared__ Stage stage_all[G::WARPS];
+  using Stage = RegStage<T, W, C>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Stage &st = stage_all[warp];
+  Stage &st = reinterpret_cast<Stage *>(smem_raw)[warp];
   const int sidx = blockIdx.x * G::WARPS + warp;
   if (sidx >= a.nsub) return;  // whole warp leaves together
   const Subproblem sp = a.sub[sidx];
@@ -154,14 +183,18 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
 #pragma unroll
       for (int u = 0; u < PER; u++) {
         const int q = lane + 32 * u;
-        const int j = bs + (q < nb ? q : 0);
-        src[u] = ld_hint(a.perm + j, pol_stream);
-        gx[u] = ld_hint(a.g1 + j, pol_stream);
-        gy[u] = ld_hint(a.g2 + j, pol_stream);
+        src[u] = 0;
+        gx[u] = gy[u] = T(0);
+        if (q < nb) {
+          src[u] = ld_hint(a.perm + bs + q, pol_stream);
+          gx[u] = ld_hint(a.g1 + bs + q, pol_stream);
+          gy[u] = ld_hint(a.g2 + bs + q, pol_stream);
+        }
       }
       CT cv[PER];
 #pragma unroll
-      for (int u = 0; u < PER; u++) cv[u] = ld_hint(a.c_in + src[u], pol_keep);
+      for (int u = 0; u < PER; u++)
+        if (lane + 32 * u < nb) cv[u] = ld_hint(a.c_in + src[u], pol_keep);
 #pragma unroll
       for (int u = 0; u < PER; u++) {
         const int q = lane + 32 * u;
@@ -169,33 +202,35 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
           T ex[G::WXP], ey[G::WXP];
           const int xb = es_extended<T, W, G::WXP>(gx[u], a.beta_e, ex);
           es_extended<T, W, G::WXP>(gy[u], a.beta_e, ey);
+          ey[G::WX] = T(xb);  // exact: |xb| < 2^24
 #pragma unroll
-          for (int s = 0; s < G::WXP; s++) st.wy[q][s] = ey[s];
+          for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::put(&st.wy[q][v], &ey[v]);
 #pragma unroll
           for (int e = 0; e < G::WXE; e++) {
             const int s = e - (C - 1);
-            st.wx[q][e] = (s >= 0 && s <= W) ? ex[s >= 0 && s <= W ? s : 0] : T(0);
+            const T wxe = (s >= 0 && s <= W) ? ex[s >= 0 && s <= W ? s : 0] : T(0);
+            CT v;
+            v.x = cv[u].x * wxe;
+            v.y = cv[u].y * wxe;
+            st.cwx[q][e] = v;
           }
-          st.c[q] = cv[u];
-          st.xb[q] = xb;
         }
       }
       __syncwarp();
       const int j0 = llo > bs ? llo : bs, j1 = lhi < bs + nb ? lhi : bs + nb;
       for (int j = j0; j < j1; j++) {
         const int q = j - bs;
-        // index of column cc's weight in the zero-padded x weights: in
-        // [0, W + 2C - 2] for points of this lane's window
-        int e0 = x0 - st.xb[q] + (C - 1);
-        e0 = e0 < 0 ? 0 : (e0 > W + C - 1 ? W + C - 1 : e0);
-        const CT cw = st.c[q];
         T wy[G::WXP];
 #pragma unroll
-        for (int s = 0; s < G::WXP; s++) wy[s] = st.wy[q][s];
+        for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::get(&st.wy[q][v], &wy[v]);
+        // index of column cc's product in the zero-padded row: in
+        // [0, W + 2C - 2] for points of this lane's window
+        int e0 = x0 - (int)wy[G::WX] + (C - 1);
+        e0 = e0 < 0 ? 0 : (e0 > W + C - 1 ? W + C - 1 : e0);
 #pragma unroll
         for (int cc = 0; cc < C; cc++) {
-          const T wx = st.wx[q][e0 + cc];
-          const T cr = cw.x * wx, ci = cw.y * wx;
+          const CT cw = st.cwx[q][e0 + cc];
+          const T cr = cw.x, ci = cw.y;
 #pragma unroll
           for (int r = 0; r < G::WX; r++) {
             acc_r[cc][r] += cr * wy[r];
@@ -256,7 +291,10 @@ cudaError_t spread_regtile2d_wc(const nufft_plan_s *p, const void *c) {
   a.cstride = p->M;
   a.gstride = grid_cells(p);
   const unsigned blocks = (unsigned)((p->nsub + G::WARPS - 1) / G::WARPS);
-  spread_regtile2d_kernel<T, W, C><<<dim3(blocks, p->nvec), 32 * G::WARPS, 0, p->stream>>>(a);
+  const size_t smem = G::WARPS * sizeof(RegStage<T, W, C>);
+  cudaError_t e = allow_smem(spread_regtile2d_kernel<T, W, C>, smem);
+  if (e != cudaSuccess) return e;
+  spread_regtile2d_kernel<T, W, C><<<dim3(blocks, p->nvec), 32 * G::WARPS, smem, p->stream>>>(a);
   return cudaGetLastError();
 }
 
