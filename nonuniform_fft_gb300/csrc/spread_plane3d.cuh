@@ -34,13 +34,18 @@ struct Plane3D {
   static constexpr int HW = W / 2;
   static constexpr int WX = W + 1;
   static constexpr int VEC = 16 / (int)sizeof(T);
-  static constexpr int WXP = (WX + VEC - 1) / VEC * VEC;
+  // staged y weights: WX values, then the point's cell offset xb in slot WX;
+  // rows an odd number of 16-byte units apart (no bank conflicts between the
+  // 8 lanes of a quarter warp storing or loading 16 bytes each)
+  static constexpr int WXP = (WX + 1 + VEC - 1) / VEC * VEC;
+  static constexpr int WYS = (WXP / VEC) % 2 == 0 ? WXP + VEC : WXP;
+  static constexpr int WCS = WX | 1;        // odd row stride of the c * x-weight products
   static constexpr int M1 = 32 - 2 * PAD;   // bin width (x)
   static constexpr int P3 = K * Z;          // padded-bin planes
   static constexpr int M3 = P3 - 2 * PAD;   // bin depth (z)
   static constexpr int THREADS = 32 * K;
   // staged points per batch: up to 256, within about 44 KB of shared memory
-  static constexpr int PT_BYTES = (int)sizeof(T) * (2 * WXP + WX) + (int)sizeof(T) * 2 + 4;
+  static constexpr int PT_BYTES = (int)sizeof(T) * (WYS + WX + 2 * WCS);
   static constexpr int S_FIT = (44 * 1024 / PT_BYTES) / 32 * 32;
   static constexpr int S = S_FIT < 256 ? S_FIT : 256;
   static_assert(S >= 32, "staging buffer too small");
@@ -70,11 +75,9 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
   using CT = typename Cplx<T>::type;
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
-  __shared__ __align__(16) T s_wy[G::S][G::WXP];
-  __shared__ __align__(16) T s_wz[G::S][G::WXP];
-  __shared__ T s_wx[G::S][G::WX];
-  __shared__ CT s_c[G::S];
-  __shared__ int s_xb[G::S];
+  __shared__ __align__(16) T s_wy[G::S][G::WYS];    // y weights; [WX]: cell offset xb
+  __shared__ T s_wz[G::S][G::WX];
+  __shared__ __align__(16) CT s_cwx[G::S][G::WCS];   // c_j times the x weights
   // runs of the current row: one per z-layer of the subproblem
   __shared__ int r_lo[G::M3], r_hi[G::M3], r_pos[G::M3 + 1];
   __shared__ int r_cs[G::M3][G::M1 + 1];
@@ -153,18 +156,22 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
         const int j = r_lo[l] + (v - r_pos[l]);
         const int q = v - vs;
         const int src = ld_hint(a.perm + j, pol_stream);
+        const CT cv = ld_hint(a.c_in + src, pol_keep);
         T ex[G::WXP], ey[G::WXP], ez[G::WXP];
-        s_xb[q] = es_extended<T, W, G::WXP>(ld_hint(a.g1 + j, pol_stream), a.beta_e, ex);
+        const int xb = es_extended<T, W, G::WXP>(ld_hint(a.g1 + j, pol_stream), a.beta_e, ex);
         es_extended<T, W, G::WXP>(ld_hint(a.g2 + j, pol_stream), a.beta_e, ey);
         es_extended<T, W, G::WXP>(ld_hint(a.g3 + j, pol_stream), a.beta_e, ez);
+        ey[G::WX] = T(xb);  // exact: |xb| < 2^24
 #pragma unroll
-        for (int s = 0; s < G::WX; s++) s_wx[q][s] = ex[s];
+        for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::put(&s_wy[q][v], &ey[v]);
 #pragma unroll
-        for (int s = 0; s < G::WXP; s++) {
-          s_wy[q][s] = ey[s];
+        for (int s = 0; s < G::WX; s++) {
           s_wz[q][s] = ez[s];
+          CT pr;
+          pr.x = cv.x * ex[s];
+          pr.y = cv.y * ex[s];
+          s_cwx[q][s] = pr;
         }
-        s_c[q] = ld_hint(a.c_in + src, pol_keep);
       }
       __syncthreads();
       // --- visit: runs whose z-window reaches this warp's planes ----------
@@ -182,18 +189,17 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
         q0 = q0 > 0 ? q0 : 0;
         q1 = q1 < ve - vs ? q1 : ve - vs;
         for (int q = q0; q < q1; q++) {
-          int d = x_rel - s_xb[q];
-          d = d < 0 ? 0 : (d > W ? W : d);
-          const T wx = s_wx[q][d];
-          const CT cv = s_c[q];
           T wy[G::WXP];
 #pragma unroll
-          for (int s = 0; s < G::WXP; s++) wy[s] = s_wy[q][s];
+          for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::get(&s_wy[q][v], &wy[v]);
+          int d = x_rel - (int)wy[G::WX];
+          d = d < 0 ? 0 : (d > W ? W : d);
+          const CT cw = s_cwx[q][d];
 #pragma unroll
           for (int i = 0; i < Z; i++) {
             const int e = ez0 + i;
             const T wz = (e >= 0 && e <= W) ? s_wz[q][e < 0 ? 0 : (e > W ? W : e)] : T(0);
-            const T cr = cv.x * wx * wz, ci = cv.y * wx * wz;
+            const T cr = cw.x * wz, ci = cw.y * wz;
 #pragma unroll
             for (int r = 0; r < G::WX; r++) {
               acc_r[i][r] += cr * wy[r];

@@ -266,6 +266,46 @@ __global__ void spread_gm_kernel(SIParams<T> a) {
 }
 
 // ---------------------------------------------------------------- SM interp
+// Interpolated value of one point from the staged padded bin (Sec. II-B c):
+// the w^d tile values around it weighted by the kernel.
+template <typename T, int DIM, int W>
+__device__ __forceinline__ typename Cplx<T>::type interp_point(const typename Cplx<T>::type *tile,
+                                                                int p1, int p2, T gx, T gy, T gz,
+                                                                T beta) {
+  using C = typename Cplx<T>::type;
+  constexpr int PAD = (W + 1) / 2;
+  T k1[W], k2[W], k3[W];
+  const int s1 = es_weights<T, W>(gx, beta, k1) + PAD;
+  const int s2 = es_weights<T, W>(gy, beta, k2) + PAD;
+  int s3 = 0;
+  if (DIM == 3) s3 = es_weights<T, W>(gz, beta, k3) + PAD;
+  T ar = T(0), ai = T(0);
+#pragma unroll 1
+  for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
+    T sr3 = T(0), si3 = T(0);
+#pragma unroll
+    for (int i2 = 0; i2 < W; i2++) {
+      const C *row = tile + ((s3 + i3) * p2 + s2 + i2) * p1 + s1;
+      T sr = T(0), si = T(0);
+#pragma unroll
+      for (int i1 = 0; i1 < W; i1++) {
+        const C b = row[i1];
+        sr += b.x * k1[i1];
+        si += b.y * k1[i1];
+      }
+      sr3 += sr * k2[i2];
+      si3 += si * k2[i2];
+    }
+    const T v3 = DIM == 3 ? k3[i3] : T(1);
+    ar += sr3 * v3;
+    ai += si3 * v3;
+  }
+  C out;
+  out.x = ar;
+  out.y = ai;
+  return out;
+}
+
 template <typename T, int DIM, int W>
 __global__ void interp_sm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
@@ -279,78 +319,84 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
   bin_coords<DIM>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
   const int p1 = a.m1 + 2 * PAD, p2 = a.m2 + 2 * PAD, p3 = DIM == 3 ? a.m3 + 2 * PAD : 1;
   const int o1 = b1 * a.m1 - PAD, o2 = b2 * a.m2 - PAD, o3 = DIM == 3 ? b3 * a.m3 - PAD : 0;
-  // stage the padded bin of the fine grid (periodic wrap) in shared memory,
-  // one tile row per warp at a time, lanes along x
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
+  const int end = sp.start + sp.count;
+  const int stride = 2 * blockDim.x;
+
+  // the first two points' coordinates and destinations are requested before
+  // the tile, so their latency overlaps the staging
+  T nx[2] = {T(0), T(0)}, ny[2] = {T(0), T(0)}, nz[2] = {T(0), T(0)};
+  int nd[2] = {0, 0};
+  int j = sp.start + threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < 2; u++) {
+    const int jj = j + u * (int)blockDim.x;
+    if (jj < end) {
+      nx[u] = ld_hint(a.g1 + jj, pol_stream);
+      ny[u] = ld_hint(a.g2 + jj, pol_stream);
+      if (DIM == 3) nz[u] = ld_hint(a.g3 + jj, pol_stream);
+      nd[u] = ld_hint(a.perm + jj, pol_stream);
+    }
+  }
+
+  // stage the padded bin of the fine grid (periodic wrap) in shared memory;
+  // each thread issues four loads before its four stores
   {
-    const int nwarps = blockDim.x >> 5, wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
-    for (int row = wid; row < p2 * p3; row += nwarps) {
-      const int s2 = row % p2, s3 = row / p2;
-      const int l2 = wrap_tile(o2 + s2, a.n2);
-      const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
-      const C *src = a.grid + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3);
-      C *dst = tile + row * p1;
-      for (int s1 = ln; s1 < p1; s1 += 32) dst[s1] = src[wrap_tile(o1 + s1, a.n1)];
+    const int cells = p1 * p2 * p3;
+    for (int base = threadIdx.x; base < cells; base += 4 * blockDim.x) {
+      C v[4];
+      int at[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int t = base + u * (int)blockDim.x;
+        at[u] = t;
+        if (t < cells) {
+          const int s1 = t % p1, r = t / p1;
+          const int s2 = r % p2, s3 = r / p2;
+          const int l1 = wrap_tile(o1 + s1, a.n1);
+          const int l2 = wrap_tile(o2 + s2, a.n2);
+          const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
+          v[u] = a.grid[l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+        if (at[u] < cells) tile[at[u]] = v[u];
     }
   }
   __syncthreads();
 
-  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
-  const int end = sp.start + sp.count;
-  // software pipeline: the next point's coordinates and destination are
-  // loaded before the current point is computed
-  int j = sp.start + threadIdx.x;
-  T nx = T(0), ny = T(0), nz = T(0);
-  int ndst = 0;
-  if (j < end) {
-    nx = ld_hint(a.g1 + j, pol_stream);
-    ny = ld_hint(a.g2 + j, pol_stream);
-    if (DIM == 3) nz = ld_hint(a.g3 + j, pol_stream);
-    ndst = ld_hint(a.perm + j, pol_stream);
-  }
-  for (; j < end; j += blockDim.x) {
-    const T gx = nx, gy = ny, gz = nz;
-    const int dst = ndst;
-    const int jn = j + blockDim.x;
-    if (jn < end) {
-      nx = ld_hint(a.g1 + jn, pol_stream);
-      ny = ld_hint(a.g2 + jn, pol_stream);
-      if (DIM == 3) nz = ld_hint(a.g3 + jn, pol_stream);
-      ndst = ld_hint(a.perm + jn, pol_stream);
+  // two points per thread and iteration, the next two prefetched
+  for (; j < end; j += stride) {
+    T gx[2], gy[2], gz[2];
+    int dst[2];
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+      gx[u] = nx[u];
+      gy[u] = ny[u];
+      gz[u] = nz[u];
+      dst[u] = nd[u];
     }
-    T k1[W], k2[W], k3[W];
-    const int s1 = es_weights<T, W>(gx, a.beta, k1) + PAD;
-    const int s2 = es_weights<T, W>(gy, a.beta, k2) + PAD;
-    int s3 = 0;
-    if (DIM == 3) s3 = es_weights<T, W>(gz, a.beta, k3) + PAD;
-    T ar = T(0), ai = T(0);
-#pragma unroll 1
-    for (int i3 = 0; i3 < (DIM == 3 ? W : 1); i3++) {
-      T sr3 = T(0), si3 = T(0);
 #pragma unroll
-      for (int i2 = 0; i2 < W; i2++) {
-        const C *row = tile + ((s3 + i3) * p2 + s2 + i2) * p1 + s1;
-        T sr = T(0), si = T(0);
-#pragma unroll
-        for (int i1 = 0; i1 < W; i1++) {
-          const C b = row[i1];
-          sr += b.x * k1[i1];
-          si += b.y * k1[i1];
-        }
-        sr3 += sr * k2[i2];
-        si3 += si * k2[i2];
+    for (int u = 0; u < 2; u++) {
+      const int jn = j + stride + u * (int)blockDim.x;
+      if (jn < end) {
+        nx[u] = ld_hint(a.g1 + jn, pol_stream);
+        ny[u] = ld_hint(a.g2 + jn, pol_stream);
+        if (DIM == 3) nz[u] = ld_hint(a.g3 + jn, pol_stream);
+        nd[u] = ld_hint(a.perm + jn, pol_stream);
       }
-      const T v3 = DIM == 3 ? k3[i3] : T(1);
-      ar += sr3 * v3;
-      ai += si3 * v3;
     }
-    C out;
-    out.x = ar;
-    out.y = ai;
-    st_hint(a.c_out + dst, out, pol_keep);
+#pragma unroll
+    for (int u = 0; u < 2; u++) {
+      if (j + u * (int)blockDim.x < end) {
+        const C out = interp_point<T, DIM, W>(tile, p1, p2, gx[u], gy[u], gz[u], a.beta);
+        st_hint(a.c_out + dst[u], out, pol_keep);
+      }
+    }
   }
 }
 
-// ---------------------------------------------------------------- GM-sort interp
 template <typename T, int DIM, int W>
 __global__ void interp_gm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
