@@ -24,6 +24,9 @@
 // no shared-memory read-modify-write.
 #pragma once
 
+#include <type_traits>
+
+#include "df64.cuh"
 #include "spread_regtile.cuh"
 
 namespace nufft {
@@ -240,14 +243,201 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
   }
 }
 
+// Double precision: the same register tile, with the multiply-accumulates in
+// two-float arithmetic (df64.cuh).  Kernel values are evaluated in double
+// per point and dimension, split once into two-floats at staging; the
+// window accumulators are two-floats and are converted back to double when a
+// row is added to the fine grid.
+template <int W, int Z, int K>
+struct Plane3DDF {
+  static constexpr int PAD = (W + 1) / 2;
+  static constexpr int HW = W / 2;
+  static constexpr int WX = W + 1;
+  static constexpr int M1 = 32 - 2 * PAD;
+  static constexpr int P3 = K * Z;
+  static constexpr int M3 = P3 - 2 * PAD;
+  static constexpr int THREADS = 32 * K;
+  static constexpr int WCS = WX | 1;  // odd stride of the 16-byte c * x-weight products
+  static constexpr int PT_BYTES = 8 * WX + 8 * WX + 16 * WCS + 4;
+  static constexpr int S_FIT = (44 * 1024 / PT_BYTES) / 32 * 32;
+  static constexpr int S = S_FIT < 256 ? S_FIT : 256;
+  static_assert(S >= 32, "staging buffer too small");
+  static_assert(M1 >= 1 && M3 >= 1, "padded bin too small for this width");
+};
+
+struct DFC {  // complex two-float
+  DF re, im;
+};
+
+template <int W, int Z, int K>
+__global__ void __launch_bounds__(Plane3DDF<W, Z, K>::THREADS, 1)
+    spread_plane3d_df_kernel(Plane3DParams<double> a) {
+  using G = Plane3DDF<W, Z, K>;
+  using CT = double2;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
+  __shared__ DF s_wy[G::S][G::WX];
+  __shared__ DF s_wz[G::S][G::WX];
+  __shared__ __align__(16) DFC s_cwx[G::S][G::WCS];   // c_j times the x weights
+  __shared__ int s_xb[G::S];
+  __shared__ int r_lo[G::M3], r_hi[G::M3], r_pos[G::M3 + 1];
+  __shared__ int r_cs[G::M3][G::M1 + 1];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Subproblem sp = a.sub[blockIdx.x];
+  const int b1 = sp.bin % a.nb1, rest = sp.bin / a.nb1;
+  const int b2 = rest % a.nb2, b3 = rest / a.nb2;
+  const int lo = sp.start, hi = sp.start + sp.count;
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
+  const int cpl = a.m1 * a.m2;
+  const int32_t *cs = a.cell_starts + (int64_t)sp.bin * cpl * a.m3;
+  const int z_a = (int)floor(a.g3[lo]);
+  const int z_b = (int)floor(a.g3[hi - 1]);
+  const int nl = z_b - z_a + 1;
+  const int t0 = warp * Z;
+  const int x_rel = lane - G::PAD;
+  int xw_lo = x_rel + G::HW - W, xw_hi = x_rel + G::HW + 1;
+  xw_lo = xw_lo < 0 ? 0 : xw_lo;
+  xw_hi = xw_hi > a.m1 ? a.m1 : xw_hi;
+  CT *col_base = a.grid + wrap_tile(b1 * a.m1 + x_rel, a.n1);
+  int64_t plane_off[Z];
+#pragma unroll
+  for (int i = 0; i < Z; i++)
+    plane_off[i] = (int64_t)wrap_tile(b3 * a.m3 - G::PAD + t0 + i, a.n3) * a.n2 * a.n1;
+  const int row0 = b2 * a.m2 - G::PAD;
+
+  DF acc_r[Z][G::WX], acc_i[Z][G::WX];
+#pragma unroll
+  for (int i = 0; i < Z; i++)
+#pragma unroll
+    for (int r = 0; r < G::WX; r++) acc_r[i][r] = acc_i[i][r] = DF{0.f, 0.f};
+
+  for (int yc = 0; yc < a.m2; yc++) {
+    for (int e = tid; e < nl * (a.m1 + 1); e += G::THREADS) {
+      const int l = e / (a.m1 + 1), x = e - l * (a.m1 + 1);
+      r_cs[l][x] = cs[((z_a + l) * a.m2 + yc) * a.m1 + x];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int len = 0;
+      if (lane < nl) {
+        int s0 = r_cs[lane][0], s1 = r_cs[lane][a.m1];
+        s0 = s0 > lo ? s0 : lo;
+        s1 = s1 < hi ? s1 : hi;
+        r_lo[lane] = s0;
+        r_hi[lane] = s1 > s0 ? s1 : s0;
+        len = s1 > s0 ? s1 - s0 : 0;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, len, o);
+        if (lane >= o) len += u;
+      }
+      if (lane < nl) r_pos[lane + 1] = len;
+      if (lane == 0) r_pos[0] = 0;
+    }
+    __syncthreads();
+    const int total = r_pos[nl];
+
+    for (int vs = 0; vs < total; vs += G::S) {
+      const int ve = vs + G::S < total ? vs + G::S : total;
+      for (int v = vs + tid; v < ve; v += G::THREADS) {
+        int l = 0;
+        while (l + 1 < nl && r_pos[l + 1] <= v) l++;
+        const int j = r_lo[l] + (v - r_pos[l]);
+        const int q = v - vs;
+        const int src = ld_hint(a.perm + j, pol_stream);
+        const CT cv = ld_hint(a.c_in + src, pol_keep);
+        const double gx = ld_hint(a.g1 + j, pol_stream), gy = ld_hint(a.g2 + j, pol_stream),
+                     gz = ld_hint(a.g3 + j, pol_stream);
+        // one dimension at a time, so only one array of kernel values is live
+        // next to the accumulators
+        double ek[G::WX];
+        es_extended<double, W, G::WX>(gy, a.beta_e, ek);
+#pragma unroll
+        for (int t = 0; t < G::WX; t++) s_wy[q][t] = df_from(ek[t]);
+        es_extended<double, W, G::WX>(gz, a.beta_e, ek);
+#pragma unroll
+        for (int t = 0; t < G::WX; t++) s_wz[q][t] = df_from(ek[t]);
+        s_xb[q] = es_extended<double, W, G::WX>(gx, a.beta_e, ek);
+#pragma unroll
+        for (int t = 0; t < G::WX; t++) {
+          DFC pr;
+          pr.re = df_from(cv.x * ek[t]);
+          pr.im = df_from(cv.y * ek[t]);
+          s_cwx[q][t] = pr;
+        }
+      }
+      __syncthreads();
+      for (int l = 0; l < nl; l++) {
+        const int zc = z_a + l;
+        const int ez0 = (t0 - G::PAD) - (zc - G::HW);
+        if (ez0 + Z - 1 < 0 || ez0 > W) continue;  // warp-uniform
+        if (xw_lo >= xw_hi) continue;
+        int j0 = r_cs[l][xw_lo], j1 = r_cs[l][xw_hi];
+        j0 = j0 > r_lo[l] ? j0 : r_lo[l];
+        j1 = j1 < r_hi[l] ? j1 : r_hi[l];
+        int q0 = r_pos[l] + (j0 - r_lo[l]) - vs, q1 = r_pos[l] + (j1 - r_lo[l]) - vs;
+        q0 = q0 > 0 ? q0 : 0;
+        q1 = q1 < ve - vs ? q1 : ve - vs;
+        for (int q = q0; q < q1; q++) {
+          int d = x_rel - s_xb[q];
+          d = d < 0 ? 0 : (d > W ? W : d);
+          const DFC cw = s_cwx[q][d];
+#pragma unroll
+          for (int i = 0; i < Z; i++) {
+            const int e = ez0 + i;
+            if (e < 0 || e > W) continue;
+            const DF wz = s_wz[q][e];
+            const DF pr = df_mul(cw.re, wz), pi = df_mul(cw.im, wz);
+#pragma unroll
+            for (int r = 0; r < G::WX; r++) {
+              const DF wy = s_wy[q][r];
+              df_fma(acc_r[i][r], pr, wy);
+              df_fma(acc_i[i][r], pi, wy);
+            }
+          }
+        }
+      }
+      __syncthreads();
+    }
+    {
+      const int64_t row_off = (int64_t)wrap_tile(row0 + yc - G::HW + G::PAD, a.n2) * a.n1;
+#pragma unroll
+      for (int i = 0; i < Z; i++) {
+        const double vr = df_to(acc_r[i][0]), vi = df_to(acc_i[i][0]);
+        if (vr != 0.0 || vi != 0.0) grid_atomic_add(col_base + plane_off[i] + row_off, vr, vi);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < Z; i++) {
+#pragma unroll
+      for (int r = 0; r < W; r++) {
+        acc_r[i][r] = acc_r[i][r + 1];
+        acc_i[i][r] = acc_i[i][r + 1];
+      }
+      acc_r[i][W] = acc_i[i][W] = DF{0.f, 0.f};
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < W; r++) {
+    const int64_t row_off = (int64_t)wrap_tile(row0 + a.m2 - G::HW + G::PAD + r, a.n2) * a.n1;
+#pragma unroll
+    for (int i = 0; i < Z; i++) {
+      const double vr = df_to(acc_r[i][r]), vi = df_to(acc_i[i][r]);
+      if (vr != 0.0 || vi != 0.0) grid_atomic_add(col_base + plane_off[i] + row_off, vr, vi);
+    }
+  }
+}
+
 // Warps per block K and planes per warp Z for a width and precision: K Z
 // padded planes, so the bin is K Z - 2 ceil(w/2) cells deep.  The register
 // windows (2 Z (w+1) values per lane) must fit K warps in one SM.
 template <typename T, int W>
 struct Plane3DChoice {
   static constexpr bool F = sizeof(T) == 4;
-  static constexpr int Z = F ? 2 : (W <= 8 ? 2 : 1);
-  static constexpr int K = F ? (W <= 8 ? 8 : 16) : (W <= 8 ? 8 : 20);
+  static constexpr int Z = F ? 2 : (W <= 8 ? 2 : 3);
+  static constexpr int K = F ? (W <= 8 ? 8 : 16) : 8;
 };
 
 template <typename T, int W>
@@ -274,7 +464,12 @@ cudaError_t spread_plane3d_w(const nufft_plan_s *p, const void *c) {
   a.nb2 = p->nb[1];
   a.cstride = p->M;
   a.gstride = grid_cells(p);
-  spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<dim3((unsigned)p->nsub, p->nvec), G::THREADS, 0, p->stream>>>(a);
+  if constexpr (std::is_same<T, double>::value) {
+    spread_plane3d_df_kernel<W, Ch::Z, Ch::K>
+        <<<dim3((unsigned)p->nsub, p->nvec), Plane3DDF<W, Ch::Z, Ch::K>::THREADS, 0, p->stream>>>(a);
+  } else {
+    spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<dim3((unsigned)p->nsub, p->nvec), G::THREADS, 0, p->stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -283,7 +478,7 @@ template <typename T>
 void plane3d_bins_t(int w, int *m1, int *m3) {
   const int pad = (w + 1) / 2;
   const bool f = sizeof(T) == 4;
-  const int z = f ? 2 : (w <= 8 ? 2 : 1), k = f ? (w <= 8 ? 8 : 16) : (w <= 8 ? 8 : 20);
+  const int z = f ? 2 : (w <= 8 ? 2 : 3), k = f ? (w <= 8 ? 8 : 16) : 8;
   *m1 = 32 - 2 * pad;
   *m3 = k * z - 2 * pad;
 }

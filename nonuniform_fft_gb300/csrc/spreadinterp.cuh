@@ -21,6 +21,9 @@
 // i.e. every node with z in [-1, 1).
 #pragma once
 
+#include <type_traits>
+
+#include "df64.cuh"
 #include "nufft_internal.cuh"
 
 namespace nufft {
@@ -397,6 +400,100 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
   }
 }
 
+// Double precision in 3D: the same staged tile and thread-per-point sums, with
+// the w^3 multiply-accumulates in two-float arithmetic (df64.cuh).  The tile
+// is converted to two-floats once when it is staged; the kernel values are
+// evaluated in double and split once per point.
+struct DFC2 {  // complex two-float, 16 bytes
+  DF re, im;
+};
+
+template <int W>
+__global__ void interp_sm3d_df_kernel(SIParams<double> a) {
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  DFC2 *tile = reinterpret_cast<DFC2 *>(smem_raw);
+  constexpr int PAD = (W + 1) / 2;
+  const Subproblem sp = a.sub[blockIdx.x];
+  int b1, b2, b3;
+  bin_coords<3>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
+  const int p1 = a.m1 + 2 * PAD, p2 = a.m2 + 2 * PAD, p3 = a.m3 + 2 * PAD;
+  const int o1 = b1 * a.m1 - PAD, o2 = b2 * a.m2 - PAD, o3 = b3 * a.m3 - PAD;
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
+  {
+    const int cells = p1 * p2 * p3;
+    for (int base = threadIdx.x; base < cells; base += 4 * blockDim.x) {
+      double2 v[4];
+      int at[4];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int t = base + u * (int)blockDim.x;
+        at[u] = t;
+        if (t < cells) {
+          const int s1 = t % p1, r = t / p1;
+          const int s2 = r % p2, s3 = r / p2;
+          const int l1 = wrap_tile(o1 + s1, a.n1);
+          const int l2 = wrap_tile(o2 + s2, a.n2);
+          const int l3 = wrap_tile(o3 + s3, a.n3);
+          v[u] = a.grid[l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; u++)
+        if (at[u] < cells) {
+          DFC2 d;
+          d.re = df_from(v[u].x);
+          d.im = df_from(v[u].y);
+          tile[at[u]] = d;
+        }
+    }
+  }
+  __syncthreads();
+  const int end = sp.start + sp.count;
+  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+    DF kx[W], ky[W], kz[W];
+    int s1, s2, s3;
+    {
+      double k[W];
+      s1 = es_weights<double, W>(ld_hint(a.g1 + j, pol_stream), a.beta, k) + PAD;
+#pragma unroll
+      for (int t = 0; t < W; t++) kx[t] = df_from(k[t]);
+      s2 = es_weights<double, W>(ld_hint(a.g2 + j, pol_stream), a.beta, k) + PAD;
+#pragma unroll
+      for (int t = 0; t < W; t++) ky[t] = df_from(k[t]);
+      s3 = es_weights<double, W>(ld_hint(a.g3 + j, pol_stream), a.beta, k) + PAD;
+#pragma unroll
+      for (int t = 0; t < W; t++) kz[t] = df_from(k[t]);
+    }
+    const int dst = ld_hint(a.perm + j, pol_stream);
+    DF ar{0.f, 0.f}, ai{0.f, 0.f};
+#pragma unroll 1
+    for (int i3 = 0; i3 < W; i3++) {
+      DF r3{0.f, 0.f}, i3s{0.f, 0.f};
+#pragma unroll
+      for (int i2 = 0; i2 < W; i2++) {
+        const DFC2 *row = tile + ((s3 + i3) * p2 + s2 + i2) * p1 + s1;
+        DF sr{0.f, 0.f}, si{0.f, 0.f};
+#pragma unroll
+        for (int i1 = 0; i1 < W; i1++) {
+          const DFC2 b = row[i1];
+          df_fma(sr, b.re, kx[i1]);
+          df_fma(si, b.im, kx[i1]);
+        }
+        df_fma(r3, sr, ky[i2]);
+        df_fma(i3s, si, ky[i2]);
+      }
+      df_fma(ar, r3, kz[i3]);
+      df_fma(ai, i3s, kz[i3]);
+    }
+    double2 out;
+    out.x = df_to(ar);
+    out.y = df_to(ai);
+    st_hint(a.c_out + dst, out, pol_keep);
+  }
+}
+
 template <typename T, int DIM, int W>
 __global__ void interp_gm_kernel(SIParams<T> a) {
   using C = typename Cplx<T>::type;
@@ -622,9 +719,15 @@ cudaError_t interp_w(const nufft_plan_s *p, void *c) {
     return cudaGetLastError();
   }
   const size_t smem = tile_cells(p) * 2 * sizeof(T);
-  cudaError_t e = allow_smem(interp_sm_kernel<T, DIM, W>, smem);
-  if (e != cudaSuccess) return e;
-  interp_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
+  if constexpr (DIM == 3 && std::is_same<T, double>::value) {
+    cudaError_t e = allow_smem(interp_sm3d_df_kernel<W>, smem);
+    if (e != cudaSuccess) return e;
+    interp_sm3d_df_kernel<W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
+  } else {
+    cudaError_t e = allow_smem(interp_sm_kernel<T, DIM, W>, smem);
+    if (e != cudaSuccess) return e;
+    interp_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
