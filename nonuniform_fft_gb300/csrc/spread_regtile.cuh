@@ -83,6 +83,23 @@ struct __align__(16) RegStage {
   typename Cplx<T>::type cwx[G::S][G::WCS];    // c_j times the x weights
 };
 
+// es_extended in two-float arithmetic (double-precision plans).
+template <int W, int WX>
+__device__ __forceinline__ int es_extended_df(double g, DF beta, DF (&ext)[WX]) {
+  constexpr int HW = W / 2;
+  const double cellf = floor(g);
+  DF k[W];
+  const int l0 = es_weights_df<W>(g, beta, k);
+  const int shift = l0 - ((int)cellf - HW);  // 0 or 1
+#pragma unroll
+  for (int s = 0; s < WX; s++) {
+    const DF v0 = s < W ? k[s < W ? s : 0] : DF{0.f, 0.f};
+    const DF v1 = (s >= 1 && s <= W) ? k[s >= 1 && s <= W ? s - 1 : 0] : DF{0.f, 0.f};
+    ext[s] = shift ? v1 : v0;
+  }
+  return (int)cellf - HW;
+}
+
 template <typename T>
 struct RegParams {
   using CT = typename Cplx<T>::type;

@@ -71,6 +71,18 @@ __device__ __forceinline__ int es_weights(T g, T beta_e, T (&k)[W]) {
   return (int)l0;
 }
 
+// The same w kernel values in two-float arithmetic (double-precision plans):
+// l0 = ceil(g - w/2) in double, then phi((l0 - g + t) 2/w) by df_es_kernel.
+template <int W>
+__device__ __forceinline__ int es_weights_df(double g, DF beta, DF (&k)[W]) {
+  const double l0 = ceil(g - 0.5 * W);
+  const DF d = df_from(l0 - g);
+  const DF scale = df_from(2.0 / W);
+#pragma unroll
+  for (int t = 0; t < W; t++) k[t] = df_es_kernel(df_mul(df_sum(d, DF{(float)t, 0.f}), scale), beta);
+  return (int)l0;
+}
+
 // L2 cache policies.  Points are streamed once per transform (evict first);
 // the caller's strengths / results are gathered or scattered through the
 // permutation, 8 or 16 bytes per 32-byte sector, so they are kept in L2
@@ -453,19 +465,10 @@ __global__ void interp_sm3d_df_kernel(SIParams<double> a) {
   const int end = sp.start + sp.count;
   for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
     DF kx[W], ky[W], kz[W];
-    int s1, s2, s3;
-    {
-      double k[W];
-      s1 = es_weights<double, W>(ld_hint(a.g1 + j, pol_stream), a.beta, k) + PAD;
-#pragma unroll
-      for (int t = 0; t < W; t++) kx[t] = df_from(k[t]);
-      s2 = es_weights<double, W>(ld_hint(a.g2 + j, pol_stream), a.beta, k) + PAD;
-#pragma unroll
-      for (int t = 0; t < W; t++) ky[t] = df_from(k[t]);
-      s3 = es_weights<double, W>(ld_hint(a.g3 + j, pol_stream), a.beta, k) + PAD;
-#pragma unroll
-      for (int t = 0; t < W; t++) kz[t] = df_from(k[t]);
-    }
+    const DF beta = df_from(a.beta);
+    const int s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), beta, kx) + PAD;
+    const int s2 = es_weights_df<W>(ld_hint(a.g2 + j, pol_stream), beta, ky) + PAD;
+    const int s3 = es_weights_df<W>(ld_hint(a.g3 + j, pol_stream), beta, kz) + PAD;
     const int dst = ld_hint(a.perm + j, pol_stream);
     DF ar{0.f, 0.f}, ai{0.f, 0.f};
 #pragma unroll 1
@@ -474,15 +477,21 @@ __global__ void interp_sm3d_df_kernel(SIParams<double> a) {
 #pragma unroll
       for (int i2 = 0; i2 < W; i2++) {
         const DFC2 *row = tile + ((s3 + i3) * p2 + s2 + i2) * p1 + s1;
-        DF sr{0.f, 0.f}, si{0.f, 0.f};
+        // two independent chains per component (even and odd i1)
+        DF sr0{0.f, 0.f}, si0{0.f, 0.f}, sr1{0.f, 0.f}, si1{0.f, 0.f};
 #pragma unroll
-        for (int i1 = 0; i1 < W; i1++) {
+        for (int i1 = 0; i1 < W; i1 += 2) {
           const DFC2 b = row[i1];
-          df_fma(sr, b.re, kx[i1]);
-          df_fma(si, b.im, kx[i1]);
+          df_fma(sr0, b.re, kx[i1]);
+          df_fma(si0, b.im, kx[i1]);
+          if (i1 + 1 < W) {
+            const DFC2 c = row[i1 + 1];
+            df_fma(sr1, c.re, kx[i1 + 1]);
+            df_fma(si1, c.im, kx[i1 + 1]);
+          }
         }
-        df_fma(r3, sr, ky[i2]);
-        df_fma(i3s, si, ky[i2]);
+        df_fma(r3, df_sum(sr0, sr1), ky[i2]);
+        df_fma(i3s, df_sum(si0, si1), ky[i2]);
       }
       df_fma(ar, r3, kz[i3]);
       df_fma(ai, i3s, kz[i3]);
@@ -673,6 +682,16 @@ inline size_t tile_cells(const nufft_plan_s *p) {
   return cells;
 }
 
+// Threads per block for a kernel: the requested count, lowered (in whole
+// warps) to what the kernel's register use allows.
+template <typename Kern>
+int block_threads(Kern kern, int requested) {
+  cudaFuncAttributes at;
+  if (cudaFuncGetAttributes(&at, kern) != cudaSuccess) return requested;
+  const int cap = at.maxThreadsPerBlock / 32 * 32;
+  return requested < cap ? requested : cap;
+}
+
 // Kernels that need more than the default 48 KB of dynamic shared memory must
 // opt in before launch.
 template <typename Kern>
@@ -688,18 +707,21 @@ cudaError_t spread_w(const nufft_plan_s *p, const void *c) {
   const unsigned blocks = (unsigned)p->nsub;
   if (p->method == NUFFT_METHOD_GM) {
     a.perm = p->bin_of;  // packed cells, caller's order
-    spread_gmu_kernel<T, DIM, W><<<dim3((unsigned)((p->M + p->threads - 1) / p->threads), p->nvec), p->threads, 0,
+    const int th = block_threads(spread_gmu_kernel<T, DIM, W>, p->threads);
+    spread_gmu_kernel<T, DIM, W><<<dim3((unsigned)((p->M + th - 1) / th), p->nvec), th, 0,
                                    p->stream>>>(a, p->M);
     return cudaGetLastError();
   }
   if (p->method == NUFFT_METHOD_GM_SORT) {
-    spread_gm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, 0, p->stream>>>(a);
+    spread_gm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), block_threads(spread_gm_kernel<T, DIM, W>, p->threads),
+                                  0, p->stream>>>(a);
     return cudaGetLastError();
   }
   const size_t smem = tile_cells(p) * 2 * sizeof(T);
   cudaError_t e = allow_smem(spread_sm_kernel<T, DIM, W>, smem);
   if (e != cudaSuccess) return e;
-  spread_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
+  spread_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), block_threads(spread_sm_kernel<T, DIM, W>, p->threads),
+                                smem, p->stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -710,23 +732,27 @@ cudaError_t interp_w(const nufft_plan_s *p, void *c) {
   const unsigned blocks = (unsigned)p->nsub;
   if (p->method == NUFFT_METHOD_GM) {
     a.perm = p->bin_of;  // packed cells, caller's order
-    interp_gmu_kernel<T, DIM, W><<<dim3((unsigned)((p->M + p->threads - 1) / p->threads), p->nvec), p->threads, 0,
+    const int th = block_threads(interp_gmu_kernel<T, DIM, W>, p->threads);
+    interp_gmu_kernel<T, DIM, W><<<dim3((unsigned)((p->M + th - 1) / th), p->nvec), th, 0,
                                    p->stream>>>(a, p->M);
     return cudaGetLastError();
   }
   if (p->method == NUFFT_METHOD_GM_SORT) {
-    interp_gm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, 0, p->stream>>>(a);
+    interp_gm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), block_threads(interp_gm_kernel<T, DIM, W>, p->threads),
+                                  0, p->stream>>>(a);
     return cudaGetLastError();
   }
   const size_t smem = tile_cells(p) * 2 * sizeof(T);
   if constexpr (DIM == 3 && std::is_same<T, double>::value) {
     cudaError_t e = allow_smem(interp_sm3d_df_kernel<W>, smem);
     if (e != cudaSuccess) return e;
-    interp_sm3d_df_kernel<W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
+    interp_sm3d_df_kernel<W><<<dim3(blocks, p->nvec), block_threads(interp_sm3d_df_kernel<W>, p->threads),
+                               smem, p->stream>>>(a);
   } else {
     cudaError_t e = allow_smem(interp_sm_kernel<T, DIM, W>, smem);
     if (e != cudaSuccess) return e;
-    interp_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), p->threads, smem, p->stream>>>(a);
+    interp_sm_kernel<T, DIM, W><<<dim3(blocks, p->nvec), block_threads(interp_sm_kernel<T, DIM, W>, p->threads),
+                                  smem, p->stream>>>(a);
   }
   return cudaGetLastError();
 }

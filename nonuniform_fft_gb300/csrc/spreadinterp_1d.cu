@@ -155,7 +155,8 @@ cudaError_t interp1d_w(const nufft_plan_s *p, void *c) {
   const size_t smem = (size_t)(p->m[0] + 2 * ((W + 1) / 2)) * 2 * sizeof(T);
   cudaError_t e = allow_smem(interp_sm1d_kernel<T, W>, smem);
   if (e != cudaSuccess) return e;
-  interp_sm1d_kernel<T, W><<<dim3((unsigned)p->nsub, p->nvec), p->threads, smem, p->stream>>>(a);
+  interp_sm1d_kernel<T, W><<<dim3((unsigned)p->nsub, p->nvec), block_threads(interp_sm1d_kernel<T, W>, p->threads),
+                             smem, p->stream>>>(a);
   return cudaGetLastError();
 }
 

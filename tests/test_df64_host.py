@@ -1,0 +1,55 @@
+"""Accuracy of the two-float (double-single) ES kernel used by the
+double-precision kernels, "cuFINUFFT: a load-balanced GPU library for
+general-purpose nonuniform FFTs" eq. (5), phi(z) = exp(beta (sqrt(1-z^2)-1)).
+The library header is compiled as host code (contraction off) and compared
+with a 40-digit evaluation by Python's decimal module."""
+import os
+import shutil
+import subprocess
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def driver(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path_factory.mktemp("df64") / "drv")
+    subprocess.run([nvcc, "-O2", "-std=c++17", "-Xcompiler", "-ffp-contract=off",
+                    os.path.join(HERE, "host", "df64_es_driver.cu"), "-o", exe],
+                   check=True, capture_output=True)
+    return exe
+
+
+def _exact(z, beta):
+    getcontext().prec = 40
+    zd, bd = Decimal(z), Decimal(beta)
+    return float((bd * ((1 - zd * zd).sqrt() - 1)).exp())
+
+
+def test_df64_es_kernel_accuracy(driver):
+    rng = np.random.default_rng(3)
+    cases = []
+    for w in range(2, 17):
+        beta = 2.30 * w
+        zs = np.concatenate([[-1.0, 1.0, 0.0, 1e-9, -0.5, 0.999999999, -0.9999], rng.uniform(-1, 1, 60)])
+        cases += [(float(z), beta) for z in zs]
+    for sigma in (1.25, 1.5):        # the sigma < 2 shapes
+        for w in (5, 9, 16):
+            beta = 2.30 * w * (4 / 3) * (1 - 0.5 / sigma)
+            cases += [(float(z), beta) for z in rng.uniform(-1, 1, 20)]
+    inp = "".join(f"{z!r} {b!r}\n" for z, b in cases)
+    out = subprocess.run([driver], input=inp, capture_output=True, text=True, check=True).stdout
+    got = [float(a) + float(b) for a, b in (line.split() for line in out.strip().splitlines())]
+    # absolute error, i.e. relative to the kernel's peak phi(0) = 1: that is
+    # the error a weighted sum sees.  A double-precision evaluation of the
+    # same formula is off by up to about beta * 1e-16 * phi (~4e-15); the
+    # two-float one carries 48 bits and stays below 8e-15.
+    for (z, beta), g in zip(cases, got):
+        ref = _exact(z, beta)
+        assert abs(g - ref) <= 8e-15, (z, beta, g, ref)

@@ -369,3 +369,15 @@ def test_widest_kernels(dim, N, eps, ttype):
         assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, eps, iflag)) <= 1e-12
         tg = np.arange(0, M, 13)
         assert oracle.rel_l2(c[tg], oracle.direct_type2(pts, fk, N, iflag, targets=tg)) <= 1e-12
+
+
+def test_threads_option_is_lowered_to_what_a_kernel_allows():
+    """1024 threads per block exceed the register budget of some kernels; the
+    launch uses the most the kernel allows instead of failing."""
+    rng = np.random.default_rng(24)
+    N = (12, 10, 8)
+    pts = _pts(3, 3000, "uniform", rng, "f64")
+    fk = _cplx(int(np.prod(N)), rng, "f64")
+    for method in (nf.METHOD_SM, nf.METHOD_GM_SORT):
+        c = gpu_transform(2, pts, fk, N, 1e-9, 1, "f64", {"threads": 1024, "method": method})
+        assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, 1e-9, 1)) <= 1e-12
