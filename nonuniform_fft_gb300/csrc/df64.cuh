@@ -7,9 +7,9 @@
 // adds, multiplies and fused multiply-adds.  This part executes about 64
 // single-precision FMAs per double-precision FMA, so the w^d
 // multiply-accumulates per point of the double-precision spreading and
-// interpolation run in this form, while the kernel values themselves are
-// evaluated in double.  Every operation uses the _rn intrinsics so the
-// compiler cannot contract or reorder the error terms.
+// interpolation run in this form, and so can the kernel values themselves
+// (df_es_kernel).  Every operation uses the _rn intrinsics so the compiler
+// cannot contract or reorder the error terms.
 #pragma once
 
 #include <cuda_runtime.h>

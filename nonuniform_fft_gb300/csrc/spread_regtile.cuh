@@ -38,7 +38,10 @@ struct RowSlide2D {
   static constexpr int WX = W + 1;          // extended window
   static constexpr int VEC = 16 / (int)sizeof(T);
   // staged y weights: WX values, then the point's cell offset xb in slot WX
-  static constexpr int WXP = (WX + 1 + VEC - 1) / VEC * VEC;
+  // when the last 16-byte unit has room for it (else in an array of its own,
+  // rather than a whole extra unit per lane-visit)
+  static constexpr bool XB_IN_ROW = WX % VEC != 0;
+  static constexpr int WXP = (WX + VEC - 1) / VEC * VEC;
   // row stride of the y weights: an odd number of 16-byte units, so that the
   // 8 lanes of a quarter warp moving 16 bytes each hit 8 different bank quads
   static constexpr int WYS = (WXP / VEC) % 2 == 0 ? WXP + VEC : WXP;
@@ -81,6 +84,7 @@ struct __align__(16) RegStage {
   using G = RowSlide2D<T, W, C>;
   T wy[G::S][G::WYS];                          // y weights; [WX]: cell offset xb
   typename Cplx<T>::type cwx[G::S][G::WCS];    // c_j times the x weights
+  int xb[G::XB_IN_ROW ? 1 : G::S];             // cell offsets, when not in wy
 };
 
 // es_extended in two-float arithmetic (double-precision plans).
@@ -219,7 +223,10 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
           T ex[G::WXP], ey[G::WXP];
           const int xb = es_extended<T, W, G::WXP>(gx[u], a.beta_e, ex);
           es_extended<T, W, G::WXP>(gy[u], a.beta_e, ey);
-          ey[G::WX] = T(xb);  // exact: |xb| < 2^24
+          if constexpr (G::XB_IN_ROW)
+            ey[G::WX] = T(xb);  // exact: |xb| < 2^24
+          else
+            st.xb[q] = xb;
 #pragma unroll
           for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::put(&st.wy[q][v], &ey[v]);
 #pragma unroll
@@ -242,7 +249,12 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
         for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::get(&st.wy[q][v], &wy[v]);
         // index of column cc's product in the zero-padded row: in
         // [0, W + 2C - 2] for points of this lane's window
-        int e0 = x0 - (int)wy[G::WX] + (C - 1);
+        int xbq;
+        if constexpr (G::XB_IN_ROW)
+          xbq = (int)wy[G::WX < G::WXP ? G::WX : 0];
+        else
+          xbq = st.xb[q];
+        int e0 = x0 - xbq + (C - 1);
         e0 = e0 < 0 ? 0 : (e0 > W + C - 1 ? W + C - 1 : e0);
 #pragma unroll
         for (int cc = 0; cc < C; cc++) {
