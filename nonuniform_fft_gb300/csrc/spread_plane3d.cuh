@@ -37,10 +37,12 @@ struct Plane3D {
   static constexpr int HW = W / 2;
   static constexpr int WX = W + 1;
   static constexpr int VEC = 16 / (int)sizeof(T);
-  // staged y weights: WX values, then the point's cell offset xb in slot WX;
-  // rows an odd number of 16-byte units apart (no bank conflicts between the
-  // 8 lanes of a quarter warp storing or loading 16 bytes each)
-  static constexpr int WXP = (WX + 1 + VEC - 1) / VEC * VEC;
+  // staged y weights: WX values, then the point's cell offset xb in slot WX
+  // when the last 16-byte unit has room (else in an array of its own); rows
+  // an odd number of 16-byte units apart (no bank conflicts between the 8
+  // lanes of a quarter warp storing or loading 16 bytes each)
+  static constexpr bool XB_IN_ROW = WX % VEC != 0;
+  static constexpr int WXP = (WX + VEC - 1) / VEC * VEC;
   static constexpr int WYS = (WXP / VEC) % 2 == 0 ? WXP + VEC : WXP;
   static constexpr int WCS = WX | 1;        // odd row stride of the c * x-weight products
   static constexpr int M1 = 32 - 2 * PAD;   // bin width (x)
@@ -48,7 +50,7 @@ struct Plane3D {
   static constexpr int M3 = P3 - 2 * PAD;   // bin depth (z)
   static constexpr int THREADS = 32 * K;
   // staged points per batch: up to 256, within about 44 KB of shared memory
-  static constexpr int PT_BYTES = (int)sizeof(T) * (WYS + WX + 2 * WCS);
+  static constexpr int PT_BYTES = (int)sizeof(T) * (WYS + WX + 2 * WCS) + (XB_IN_ROW ? 0 : 4);
   static constexpr int S_FIT = (44 * 1024 / PT_BYTES) / 32 * 32;
   static constexpr int S = S_FIT < 256 ? S_FIT : 256;
   static_assert(S >= 32, "staging buffer too small");
@@ -80,6 +82,7 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
   a.c_in += blockIdx.y * a.cstride;
   __shared__ __align__(16) T s_wy[G::S][G::WYS];    // y weights; [WX]: cell offset xb
   __shared__ T s_wz[G::S][G::WX];
+  __shared__ int s_xbs[G::XB_IN_ROW ? 1 : G::S];    // cell offsets, when not in s_wy
   __shared__ __align__(16) CT s_cwx[G::S][G::WCS];   // c_j times the x weights
   // runs of the current row: one per z-layer of the subproblem
   __shared__ int r_lo[G::M3], r_hi[G::M3], r_pos[G::M3 + 1];
@@ -164,7 +167,10 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
         const int xb = es_extended<T, W, G::WXP>(ld_hint(a.g1 + j, pol_stream), a.beta_e, ex);
         es_extended<T, W, G::WXP>(ld_hint(a.g2 + j, pol_stream), a.beta_e, ey);
         es_extended<T, W, G::WXP>(ld_hint(a.g3 + j, pol_stream), a.beta_e, ez);
-        ey[G::WX] = T(xb);  // exact: |xb| < 2^24
+        if constexpr (G::XB_IN_ROW)
+          ey[G::WX < G::WXP ? G::WX : 0] = T(xb);  // exact: |xb| < 2^24
+        else
+          s_xbs[q] = xb;
 #pragma unroll
         for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::put(&s_wy[q][v], &ey[v]);
 #pragma unroll
@@ -195,7 +201,11 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
           T wy[G::WXP];
 #pragma unroll
           for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::get(&s_wy[q][v], &wy[v]);
-          int d = x_rel - (int)wy[G::WX];
+          int d;
+          if constexpr (G::XB_IN_ROW)
+            d = x_rel - (int)wy[G::WX < G::WXP ? G::WX : 0];
+          else
+            d = x_rel - s_xbs[q];
           d = d < 0 ? 0 : (d > W ? W : d);
           const CT cw = s_cwx[q][d];
 #pragma unroll
