@@ -14,7 +14,9 @@
 //     column into the fine grid (eq. (15)).
 //   * Interpolation: one block per subproblem stages the padded bin of the
 //     fine grid in shared memory, one thread per point reads its w nodes.
-#include "spreadinterp.cuh"
+#include <type_traits>
+
+#include "spread_regtile.cuh"
 
 namespace nufft {
 namespace {
@@ -87,6 +89,64 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_kernel(Params1D<T>
     grid_atomic_add(a.grid + wrap_tile(sp.bin * a.m1 + x_rel, a.n1), ar, ai);
 }
 
+// Double precision: each point's w+1 extended kernel values are evaluated
+// once, in two-float arithmetic (df64.cuh), when its batch is staged, and
+// stored as products c_j phi; a lane-visit is then one 16-byte load and two
+// adds (evaluating the kernel per lane-visit in double cost w+1 double
+// exp/sqrt pairs per point on this part's small FP64 rate).
+template <int W>
+__global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_df_kernel(Params1D<double> a) {
+  constexpr int PAD = (W + 1) / 2, HW = W / 2, WX = W + 1, WCS = WX | 1;
+  constexpr int S = W <= 8 ? 64 : 32;
+  __shared__ double2 s_cw[kWarps1D][S][WCS];
+  __shared__ int s_xb[kWarps1D][S];
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_in += blockIdx.y * a.cstride;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sidx = blockIdx.x * kWarps1D + warp;
+  if (sidx >= a.nsub) return;  // whole warp leaves together
+  const Subproblem sp = a.sub[sidx];
+  const int lo = sp.start, hi = sp.start + sp.count;
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
+  const int32_t *cs = a.cell_starts + (int64_t)sp.bin * a.m1;
+  const int x_rel = lane - PAD;
+  int xw_lo = x_rel + HW - W, xw_hi = x_rel + HW + 1;
+  xw_lo = xw_lo < 0 ? 0 : xw_lo;
+  xw_hi = xw_hi > a.m1 ? a.m1 : xw_hi;
+  int llo = hi, lhi = hi;
+  if (xw_lo < xw_hi) {
+    llo = cs[xw_lo] > lo ? cs[xw_lo] : lo;
+    lhi = cs[xw_hi] < hi ? cs[xw_hi] : hi;
+  }
+  const DF beta = df_from(a.beta_e);
+  double ar = 0.0, ai = 0.0;
+  for (int bs = lo; bs < hi; bs += S) {
+    const int nb = (bs + S < hi ? bs + S : hi) - bs;
+    for (int q = lane; q < nb; q += 32) {
+      const double2 cv = ld_hint(a.c_in + ld_hint(a.perm + bs + q, pol_stream), pol_keep);
+      DF ext[WX];
+      s_xb[warp][q] = es_extended_df<W, WX>(ld_hint(a.g1 + bs + q, pol_stream), beta, ext);
+#pragma unroll
+      for (int e = 0; e < WX; e++) {
+        const double w = df_to(ext[e]);
+        s_cw[warp][q][e] = make_double2(cv.x * w, cv.y * w);
+      }
+    }
+    __syncwarp();
+    const int j0 = llo > bs ? llo : bs, j1 = lhi < bs + nb ? lhi : bs + nb;
+    for (int j = j0; j < j1; j++) {
+      const int q = j - bs;
+      int e = x_rel - s_xb[warp][q];
+      e = e < 0 ? 0 : (e > W ? W : e);
+      const double2 v = s_cw[warp][q][e];
+      ar += v.x;
+      ai += v.y;
+    }
+    __syncwarp();
+  }
+  if (ar != 0.0 || ai != 0.0) grid_atomic_add(a.grid + wrap_tile(sp.bin * a.m1 + x_rel, a.n1), ar, ai);
+}
+
 template <typename T, int W>
 __global__ void interp_sm1d_kernel(Params1D<T> a) {
   using CT = typename Cplx<T>::type;
@@ -104,7 +164,15 @@ __global__ void interp_sm1d_kernel(Params1D<T> a) {
   const int end = sp.start + sp.count;
   for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
     T k1[W];
-    const int s1 = es_weights<T, W>(ld_hint(a.g1 + j, pol_stream), a.beta_e, k1) + PAD;
+    int s1;
+    if constexpr (std::is_same<T, double>::value) {
+      DF kd[W];
+      s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), df_from(a.beta_e), kd) + PAD;
+#pragma unroll
+      for (int t = 0; t < W; t++) k1[t] = df_to(kd[t]);
+    } else {
+      s1 = es_weights<T, W>(ld_hint(a.g1 + j, pol_stream), a.beta_e, k1) + PAD;
+    }
     T ar = T(0), ai = T(0);
 #pragma unroll
     for (int i1 = 0; i1 < W; i1++) {
@@ -142,7 +210,12 @@ template <typename T, int W>
 cudaError_t spread1d_w(const nufft_plan_s *p, const void *c) {
   Params1D<T> a = params1d<T>(p);
   a.c_in = static_cast<const typename Cplx<T>::type *>(c);
-  spread_reg1d_kernel<T, W><<<dim3((unsigned)((p->nsub + kWarps1D - 1) / kWarps1D), p->nvec),
+  const dim3 grid((unsigned)((p->nsub + kWarps1D - 1) / kWarps1D), p->nvec);
+  if constexpr (std::is_same<T, double>::value) {
+    spread_reg1d_df_kernel<W><<<grid, 32 * kWarps1D, 0, p->stream>>>(a);
+    return cudaGetLastError();
+  }
+  spread_reg1d_kernel<T, W><<<grid,
                               32 * kWarps1D, 0,
                               p->stream>>>(a);
   return cudaGetLastError();
