@@ -281,10 +281,12 @@ def run_ours(args, wl):
     p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
                  **opts)
     p1.setpts(*xs)
+    p1.setpts(*xs)    # the "setpts" scope is this second call: buffers already allocated
     p2 = None
     if 2 in wl.types:
         p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
                      **opts)
+        p2.setpts(*xs)
         p2.setpts(*xs)
     info = p1.info()
     n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
@@ -402,7 +404,8 @@ def run_ours(args, wl):
     # (setpts + exec, on the device) and "total+mem" (host arrays in and out,
     # setpts and exec, wall clock, synchronous)
     setpts_ms = p1.timings()["setpts"] + (p2.timings()["setpts"] if has2 else 0.0)
-    scopes = {"exec_ms": t_max / K, "setpts_ms": setpts_ms, "total_ms": t_max / K + setpts_ms}
+    scopes = {"exec_ms": t_max / K, "setpts_ms": setpts_ms, "total_ms": t_max / K + setpts_ms,
+              "setpts_note": "device time of a second setpts per plan (buffers allocated)"}
     if not args.no_e2e:
         hx = [x.cpu().pin_memory() for x in xs]
         torch.cuda.synchronize()

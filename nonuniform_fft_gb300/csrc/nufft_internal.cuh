@@ -82,6 +82,8 @@ struct nufft_plan_s {
   int32_t *bin_of = nullptr;       // M (setpts scratch: each point's cell key)
   int32_t *rank_of = nullptr;      // M (setpts scratch)
   int64_t cap_pts = 0;
+  void *gtmp = nullptr;            // setpts scratch: dim x M bin-relative coordinates, caller order
+  int64_t cap_gtmp = 0;
   nufft::Subproblem *subprob = nullptr;
   int64_t cap_sub = 0;
   int *flag = nullptr;             // device error flag (setpts)

@@ -194,6 +194,7 @@ void release(nufft_plan_s *p) {
   cudaFree(p->perm);
   cudaFree(p->bin_of);
   cudaFree(p->rank_of);
+  cudaFree(p->gtmp);
   cudaFree(p->subprob);
   cudaFree(p->flag);
   cudaFree(p->stage_c);

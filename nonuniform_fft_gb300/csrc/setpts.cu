@@ -87,15 +87,23 @@ __global__ void permute_kernel(PointsIn a, const int32_t *starts, const int32_t 
   }
 }
 
+__device__ __forceinline__ float below(float v) { return nextafterf(v, 0.0f); }
+__device__ __forceinline__ double below(double v) { return ::nextafter(v, 0.0); }
+
 // Cell-level key of a point: its bin, then its cell inside the bin (x fastest).
 // Sorting by this key orders the points bin by bin (as Sec. III-A) and, inside
 // each bin, cell by cell, so a bin's points of one fine-grid row (and one x
 // range of that row) form a contiguous run.
+// The fold to the fine grid is done once, here: the point's bin-relative
+// coordinate, rounded to T but never up to the next cell (floor stays the
+// point's cell), is written in the caller's order to rel_d and later gathered
+// into sorted order.
 template <typename T>
 __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, int32_t *rank_of,
-                                  int *flag) {
+                                  int *flag, T *rel0, T *rel1, T *rel2) {
   const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= a.M) return;
+  T *out[3] = {rel0, rel1, rel2};
   bool bad = false;
   int bin = 0, stride = 1, local = 0, lstride = 1;
   for (int d = 0; d < a.dim; d++) {
@@ -103,10 +111,14 @@ __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, 
     int cell = (int)floor(g);
     if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
     const int b = cell / a.m[d];
+    const int cell_rel = cell - b * a.m[d];
     bin += b * stride;
     stride *= a.nb[d];
-    local += (cell - b * a.m[d]) * lstride;
+    local += cell_rel * lstride;
     lstride *= a.m[d];
+    T v = (T)(g - (double)(b * a.m[d]));  // exact in double, then rounded to T
+    if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
+    out[d][j] = v;
   }
   if (bad) atomicOr(flag, 1);
   const int32_t key = bin * lstride + local;
@@ -114,30 +126,25 @@ __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, 
   rank_of[j] = atomicAdd(&counts[key], 1);
 }
 
-__device__ __forceinline__ float below(float v) { return nextafterf(v, 0.0f); }
-__device__ __forceinline__ double below(double v) { return ::nextafter(v, 0.0); }
-
-// Sorted slot of each point; its bin-relative coordinate, rounded to T but
-// never up to the next cell (floor(g) stays the point's cell).
-template <typename T>
-__global__ void cell_permute_kernel(PointsIn a, const int32_t *starts, const int32_t *key_of,
-                                    const int32_t *rank_of, int32_t *perm, T *g0, T *g1, T *g2) {
+// Sorted slot of each point: the one scattered store of the sort.
+__global__ void cell_scatter_kernel(int64_t M, const int32_t *starts, const int32_t *key_of,
+                                    const int32_t *rank_of, int32_t *perm) {
   const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= a.M) return;
-  const int32_t pos = starts[key_of[j]] + rank_of[j];
-  perm[pos] = (int32_t)j;
-  T *out[3] = {g0, g1, g2};
-  bool bad = false;
-  for (int d = 0; d < a.dim; d++) {
-    double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
-    int cell = (int)floor(g);
-    if (cell >= a.n[d]) cell = a.n[d] - 1;
-    const int cell_rel = cell - (cell / a.m[d]) * a.m[d];
-    const double rel = g - (double)((cell / a.m[d]) * a.m[d]);  // exact
-    T v = (T)rel;
-    if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
-    out[d][pos] = v;
-  }
+  if (j >= M) return;
+  perm[starts[key_of[j]] + rank_of[j]] = (int32_t)j;
+}
+
+// Bin-relative coordinates in sorted order: coalesced writes, reads gathered
+// through the permutation (the caller-order arrays stay in L2).
+template <typename T>
+__global__ void gather_coords_kernel(int64_t M, int dim, const int32_t *perm, const T *rel0,
+                                     const T *rel1, const T *rel2, T *g0, T *g1, T *g2) {
+  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= M) return;
+  const int32_t j = perm[q];
+  g0[q] = rel0[j];
+  if (dim >= 2) g1[q] = rel1[j];
+  if (dim == 3) g2[q] = rel2[j];
 }
 
 // Bin counts and starts from the cell starts (cpb cells per bin).
@@ -271,6 +278,9 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     p->cap_pts = M;
   }
   if (!p->flag && cudaMalloc((void **)&p->flag, sizeof(int)) != cudaSuccess) return NUFFT_ERR_ALLOC;
+  // caller-order bin-relative coordinates (dim arrays of M reals)
+  if (grow(&p->gtmp, &p->cap_gtmp, (int64_t)p->dim * (M > 0 ? M : 1), rs) != cudaSuccess)
+    return NUFFT_ERR_ALLOC;
 
   // --- 1. cells, bins and counts ------------------------------------------
   PointsIn a;
@@ -291,11 +301,16 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     return NUFFT_ERR_CUDA;
   const int threads = 256;
   const unsigned blocks_pts = (unsigned)((M + threads - 1) / threads);
+  void *rel[3];
+  for (int d = 0; d < 3; d++)
+    rel[d] = static_cast<char *>(p->gtmp) + (size_t)(d < p->dim ? d : 0) * (size_t)M * rs;
   if (M > 0) {
     if (p->dtype == 0)
-      cell_count_kernel<float><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag);
+      cell_count_kernel<float><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag,
+                                                             (float *)rel[0], (float *)rel[1], (float *)rel[2]);
     else
-      cell_count_kernel<double><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag);
+      cell_count_kernel<double><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag,
+                                                              (double *)rel[0], (double *)rel[1], (double *)rel[2]);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
@@ -309,14 +324,16 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
 
   // --- 3. permutation and sorted coordinates ------------------------------
   if (M > 0) {
+    cell_scatter_kernel<<<blocks_pts, threads, 0, s>>>(M, p->cell_starts, p->bin_of, p->rank_of, p->perm);
+    void *g1 = p->dim >= 2 ? p->gcoord[1] : p->gcoord[0], *g2 = p->dim == 3 ? p->gcoord[2] : p->gcoord[0];
     if (p->dtype == 0)
-      cell_permute_kernel<float><<<blocks_pts, threads, 0, s>>>(
-          a, p->cell_starts, p->bin_of, p->rank_of, p->perm, (float *)p->gcoord[0],
-          (float *)p->gcoord[1], (float *)(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]));
+      gather_coords_kernel<float><<<blocks_pts, threads, 0, s>>>(
+          M, p->dim, p->perm, (const float *)rel[0], (const float *)rel[1], (const float *)rel[2],
+          (float *)p->gcoord[0], (float *)g1, (float *)g2);
     else
-      cell_permute_kernel<double><<<blocks_pts, threads, 0, s>>>(
-          a, p->cell_starts, p->bin_of, p->rank_of, p->perm, (double *)p->gcoord[0],
-          (double *)p->gcoord[1], (double *)(p->dim == 3 ? p->gcoord[2] : p->gcoord[0]));
+      gather_coords_kernel<double><<<blocks_pts, threads, 0, s>>>(
+          M, p->dim, p->perm, (const double *)rel[0], (const double *)rel[1], (const double *)rel[2],
+          (double *)p->gcoord[0], (double *)g1, (double *)g2);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
