@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
 // per point and dimension, split once into two-floats at staging; the
 // window accumulators are two-floats and are converted back to double when a
 // row is added to the fine grid.
-template <int W, int Z, int K>
+template <int W, int Z, int K, int STAGE_KB = 160>
 struct Plane3DDF {
   static constexpr int PAD = (W + 1) / 2;
   static constexpr int HW = W / 2;
@@ -268,9 +268,12 @@ struct Plane3DDF {
   static constexpr int M3 = P3 - 2 * PAD;
   static constexpr int THREADS = 32 * K;
   static constexpr int WCS = WX | 1;  // odd stride of the 16-byte c * x-weight products
+  // staged points per batch: the accumulators allow one block per SM, so the
+  // staging buffer (dynamic shared memory) may take most of the SM's 228 KB;
+  // fewer, larger batches mean fewer block barriers per bin row
   static constexpr int PT_BYTES = 8 * WX + 8 * WX + 16 * WCS + 4;
-  static constexpr int S_FIT = (44 * 1024 / PT_BYTES) / 32 * 32;
-  static constexpr int S = S_FIT < 256 ? S_FIT : 256;
+  static constexpr int S_FIT = (STAGE_KB * 1024 / PT_BYTES) / 32 * 32;
+  static constexpr int S = S_FIT < 1024 ? S_FIT : 1024;
   static_assert(S >= 32, "staging buffer too small");
   static_assert(M1 >= 1 && M3 >= 1, "padded bin too small for this width");
 };
@@ -280,16 +283,27 @@ struct DFC {  // complex two-float
 };
 
 template <int W, int Z, int K>
+struct __align__(16) Plane3DDFStage {
+  using G = Plane3DDF<W, Z, K>;
+  DFC cwx[G::S][G::WCS];  // c_j times the x weights
+  DF wy[G::S][G::WX];
+  DF wz[G::S][G::WX];
+  int xb[G::S];
+};
+
+template <int W, int Z, int K>
 __global__ void __launch_bounds__(Plane3DDF<W, Z, K>::THREADS, 1)
     spread_plane3d_df_kernel(Plane3DParams<double> a) {
   using G = Plane3DDF<W, Z, K>;
   using CT = double2;
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
-  __shared__ DF s_wy[G::S][G::WX];
-  __shared__ DF s_wz[G::S][G::WX];
-  __shared__ __align__(16) DFC s_cwx[G::S][G::WCS];   // c_j times the x weights
-  __shared__ int s_xb[G::S];
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Plane3DDFStage<W, Z, K> &stg = *reinterpret_cast<Plane3DDFStage<W, Z, K> *>(smem_raw);
+  auto &s_wy = stg.wy;
+  auto &s_wz = stg.wz;
+  auto &s_cwx = stg.cwx;
+  auto &s_xb = stg.xb;
   __shared__ int r_lo[G::M3], r_hi[G::M3], r_pos[G::M3 + 1];
   __shared__ int r_cs[G::M3][G::M1 + 1];
 
@@ -477,8 +491,11 @@ cudaError_t spread_plane3d_w(const nufft_plan_s *p, const void *c) {
   a.cstride = p->M;
   a.gstride = grid_cells(p);
   if constexpr (std::is_same<T, double>::value) {
+    const size_t smem = sizeof(Plane3DDFStage<W, Ch::Z, Ch::K>);
+    const cudaError_t e = allow_smem(spread_plane3d_df_kernel<W, Ch::Z, Ch::K>, smem);
+    if (e != cudaSuccess) return e;
     spread_plane3d_df_kernel<W, Ch::Z, Ch::K>
-        <<<dim3((unsigned)p->nsub, p->nvec), Plane3DDF<W, Ch::Z, Ch::K>::THREADS, 0, p->stream>>>(a);
+        <<<dim3((unsigned)p->nsub, p->nvec), Plane3DDF<W, Ch::Z, Ch::K>::THREADS, smem, p->stream>>>(a);
   } else {
     spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<dim3((unsigned)p->nsub, p->nvec), G::THREADS, 0, p->stream>>>(a);
   }
