@@ -31,7 +31,7 @@
 
 namespace nufft {
 
-template <typename T, int W, int Z, int K>
+template <typename T, int W, int Z, int K, int STAGE_KB = 72>
 struct Plane3D {
   static constexpr int PAD = (W + 1) / 2;
   static constexpr int HW = W / 2;
@@ -49,12 +49,22 @@ struct Plane3D {
   static constexpr int P3 = K * Z;          // padded-bin planes
   static constexpr int M3 = P3 - 2 * PAD;   // bin depth (z)
   static constexpr int THREADS = 32 * K;
-  // staged points per batch: up to 256, within about 44 KB of shared memory
+  // staged points per batch within STAGE_KB of dynamic shared memory (three
+  // blocks of 8 warps share an SM); larger batches mean fewer block barriers
   static constexpr int PT_BYTES = (int)sizeof(T) * (WYS + WX + 2 * WCS) + (XB_IN_ROW ? 0 : 4);
-  static constexpr int S_FIT = (44 * 1024 / PT_BYTES) / 32 * 32;
-  static constexpr int S = S_FIT < 256 ? S_FIT : 256;
+  static constexpr int S_FIT = (STAGE_KB * 1024 / PT_BYTES) / 32 * 32;
+  static constexpr int S = S_FIT < 1024 ? S_FIT : 1024;
   static_assert(S >= 32, "staging buffer too small");
   static_assert(M1 >= 1 && M3 >= 1, "padded bin too small for this width");
+};
+
+template <typename T, int W, int Z, int K>
+struct __align__(16) Plane3DStage {
+  using G = Plane3D<T, W, Z, K>;
+  typename Cplx<T>::type cwx[G::S][G::WCS];
+  T wy[G::S][G::WYS];
+  T wz[G::S][G::WX];
+  int xb[G::XB_IN_ROW ? 1 : G::S];
 };
 
 template <typename T>
@@ -80,10 +90,12 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
   using CT = typename Cplx<T>::type;
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
-  __shared__ __align__(16) T s_wy[G::S][G::WYS];    // y weights; [WX]: cell offset xb
-  __shared__ T s_wz[G::S][G::WX];
-  __shared__ int s_xbs[G::XB_IN_ROW ? 1 : G::S];    // cell offsets, when not in s_wy
-  __shared__ __align__(16) CT s_cwx[G::S][G::WCS];   // c_j times the x weights
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Plane3DStage<T, W, Z, K> &stg = *reinterpret_cast<Plane3DStage<T, W, Z, K> *>(smem_raw);
+  auto &s_wy = stg.wy;    // y weights; [WX]: cell offset xb
+  auto &s_wz = stg.wz;
+  auto &s_xbs = stg.xb;   // cell offsets, when not in s_wy
+  auto &s_cwx = stg.cwx;  // c_j times the x weights
   // runs of the current row: one per z-layer of the subproblem
   __shared__ int r_lo[G::M3], r_hi[G::M3], r_pos[G::M3 + 1];
   __shared__ int r_cs[G::M3][G::M1 + 1];
@@ -497,7 +509,10 @@ cudaError_t spread_plane3d_w(const nufft_plan_s *p, const void *c) {
     spread_plane3d_df_kernel<W, Ch::Z, Ch::K>
         <<<dim3((unsigned)p->nsub, p->nvec), Plane3DDF<W, Ch::Z, Ch::K>::THREADS, smem, p->stream>>>(a);
   } else {
-    spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<dim3((unsigned)p->nsub, p->nvec), G::THREADS, 0, p->stream>>>(a);
+    const size_t smem = sizeof(Plane3DStage<T, W, Ch::Z, Ch::K>);
+    const cudaError_t e = allow_smem(spread_plane3d_kernel<T, W, Ch::Z, Ch::K>, smem);
+    if (e != cudaSuccess) return e;
+    spread_plane3d_kernel<T, W, Ch::Z, Ch::K><<<dim3((unsigned)p->nsub, p->nvec), G::THREADS, smem, p->stream>>>(a);
   }
   return cudaGetLastError();
 }
