@@ -146,7 +146,7 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *   "threads"  threads per block of the SM / GM-sort spreading and
  *              interpolation kernels (multiple of 32, 32..1024; lowered to
  *              what a kernel's register use allows).  Default 256, and 512
- *              for the double-precision 3D shared-memory interpolator.
+ *              for the 3D shared-memory interpolators.
  *   "batch"    vectors per pass of nufft_execute_batch, 1..1024 (0: as many
  *              fine grids as fit in 1 GiB, at most 64).  Takes effect at the
  *              next execute.

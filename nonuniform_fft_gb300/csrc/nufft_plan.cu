@@ -464,10 +464,10 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   if (p->method == NUFFT_METHOD_GM && nufft::grid_cells(p) >= (int64_t(1) << 31)) return NUFFT_ERR_TOO_LARGE;
   // the cell-level sort indexes (bin, cell) pairs with int32
   if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
-  // the double-precision 3D interpolator holds one large tile per block: more
-  // threads per block keep more warps per SM busy
-  const int def_threads =
-      (p->dim == 3 && p->dtype == 1 && p->type == 2 && p->method == NUFFT_METHOD_SM) ? 512 : 256;
+  // the 3D interpolators hold one large tile per block (two blocks per SM in
+  // single precision, one in double): more threads per block keep more warps
+  // per SM busy
+  const int def_threads = (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM) ? 512 : 256;
   p->threads = p->opt_threads > 0 ? p->opt_threads : def_threads;
   p->M = M;
 

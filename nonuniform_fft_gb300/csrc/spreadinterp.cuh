@@ -412,6 +412,102 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
   }
 }
 
+// Single precision in 3D: the staged tile and thread-per-point sums of
+// interp_sm_kernel, with the subproblem's points taken in a bank-spread
+// order.  A point's w^3 tile reads all fall on bank pair (window origin +
+// common offset) mod 16, so 16 lanes of a half warp whose window origins are
+// distinct mod 16 read without bank conflicts.  The block buckets its points
+// by origin mod 16 (a counting sort in shared memory) and walks the
+// bucket-sorted list with a stride close to n / 16 and coprime with n, so
+// consecutive lanes take points from consecutive buckets.  In cell order the
+// windows of neighbouring points start on different rows and planes, and the
+// loads average 4.5 wavefronts per warp instruction instead of 2.
+template <int W>
+__global__ void interp_sm3d_bank_kernel(SIParams<float> a) {
+  using C = float2;
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  constexpr int PAD = (W + 1) / 2;
+  const Subproblem sp = a.sub[blockIdx.x];
+  int b1, b2, b3;
+  bin_coords<3>(sp.bin, a.nb1, a.nb2, b1, b2, b3);
+  const int p1 = a.m1 + 2 * PAD, p2 = a.m2 + 2 * PAD, p3 = a.m3 + 2 * PAD;
+  const int o1 = b1 * a.m1 - PAD, o2 = b2 * a.m2 - PAD, o3 = b3 * a.m3 - PAD;
+  const int cells = p1 * p2 * p3;
+  C *tile = reinterpret_cast<C *>(smem_raw);
+  int *order = reinterpret_cast<int *>(tile + cells);  // sp.count entries
+  __shared__ int cnt[16], cur[16], step_s;
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
+  const int n = sp.count;
+  if (threadIdx.x < 16) cnt[threadIdx.x] = 0;
+  for (int base = threadIdx.x; base < cells; base += 4 * blockDim.x) {
+    C v[4];
+    int at[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int t = base + u * (int)blockDim.x;
+      at[u] = t;
+      if (t < cells) {
+        const int s1 = t % p1, rr = t / p1;
+        const int s2 = rr % p2, s3 = rr / p2;
+        v[u] = a.grid[wrap_tile(o1 + s1, a.n1) +
+                      (int64_t)a.n1 * (wrap_tile(o2 + s2, a.n2) + (int64_t)a.n2 * wrap_tile(o3 + s3, a.n3))];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; u++)
+      if (at[u] < cells) tile[at[u]] = v[u];
+  }
+  __syncthreads();
+  // window origin of a point in the tile, and its bank pair
+  auto origin = [&](int k) {
+    const int j = sp.start + k;
+    const int s1 = (int)es_ceil(a.g1[j] - 0.5f * W) + PAD;
+    const int s2 = (int)es_ceil(a.g2[j] - 0.5f * W) + PAD;
+    const int s3 = (int)es_ceil(a.g3[j] - 0.5f * W) + PAD;
+    return (s3 * p2 + s2) * p1 + s1;
+  };
+  for (int k = threadIdx.x; k < n; k += blockDim.x) atomicAdd(&cnt[origin(k) & 15], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < 16; b++) {
+      cur[b] = acc;
+      acc += cnt[b];
+    }
+    int st = n / 16 > 0 ? n / 16 : 1;
+    auto gcd = [](int x, int y) {
+      while (y) {
+        const int t = x % y;
+        x = y;
+        y = t;
+      }
+      return x;
+    };
+    while (gcd(st, n) != 1) st++;
+    step_s = st;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k < n; k += blockDim.x) order[atomicAdd(&cur[origin(k) & 15], 1)] = k;
+  __syncthreads();
+
+  const int step = step_s;
+  // slot s takes order[(s step) mod n], updated incrementally
+  int idx = n > 0 ? (int)(((int64_t)threadIdx.x * step) % n) : 0;
+  const int inc = n > 0 ? (int)(((int64_t)blockDim.x * step) % n) : 0;
+  for (int slot = threadIdx.x; slot < n; slot += blockDim.x) {
+    const int k = order[idx];
+    idx += inc;
+    if (idx >= n) idx -= n;
+    const int j = sp.start + k;
+    const C out = interp_point<float, 3, W>(tile, p1, p2, ld_hint(a.g1 + j, pol_stream),
+                                            ld_hint(a.g2 + j, pol_stream), ld_hint(a.g3 + j, pol_stream),
+                                            a.beta);
+    st_hint(a.c_out + ld_hint(a.perm + j, pol_stream), out, pol_keep);
+  }
+}
+
 // Double precision in 3D: the same staged tile and thread-per-point sums, with
 // the w^3 multiply-accumulates in two-float arithmetic (df64.cuh).  The tile
 // is converted to two-floats once when it is staged; the kernel values are
@@ -743,6 +839,14 @@ cudaError_t interp_w(const nufft_plan_s *p, void *c) {
     return cudaGetLastError();
   }
   const size_t smem = tile_cells(p) * 2 * sizeof(T);
+  if constexpr (DIM == 3 && std::is_same<T, float>::value) {
+    const size_t smem_bk = smem + (size_t)p->msub * sizeof(int);
+    cudaError_t e = allow_smem(interp_sm3d_bank_kernel<W>, smem_bk);
+    if (e != cudaSuccess) return e;
+    interp_sm3d_bank_kernel<W><<<dim3(blocks, p->nvec), block_threads(interp_sm3d_bank_kernel<W>, p->threads),
+                                 smem_bk, p->stream>>>(a);
+    return cudaGetLastError();
+  }
   if constexpr (DIM == 3 && std::is_same<T, double>::value) {
     cudaError_t e = allow_smem(interp_sm3d_df_kernel<W>, smem);
     if (e != cudaSuccess) return e;
