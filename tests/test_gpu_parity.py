@@ -381,3 +381,22 @@ def test_threads_option_is_lowered_to_what_a_kernel_allows():
     for method in (nf.METHOD_SM, nf.METHOD_GM_SORT):
         c = gpu_transform(2, pts, fk, N, 1e-9, 1, "f64", {"threads": 1024, "method": method})
         assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, 1e-9, 1)) <= 1e-12
+
+
+@pytest.mark.parametrize("dim,N", [(1, (700,)), (2, (70, 46)), (3, (30, 22, 26))])
+@pytest.mark.parametrize("dt,eps", [("f32", 1e-5), ("f64", 1e-12)])
+@pytest.mark.parametrize("msub", [0, 37])
+def test_interp_clustered_and_ragged(dim, N, dt, eps, msub):
+    """Type 2 with half the points in one cluster (many subproblems in a few
+    bins), grids that are not a multiple of the bin size, and an odd M_sub
+    (subproblems of 37 points: the 3D single-precision interpolator walks its
+    bank-sorted points with a stride coprime with 37)."""
+    rng = np.random.default_rng(43)
+    M = 30000
+    pts = _pts(dim, M, "uniform", rng, dt)
+    for a in pts:
+        a[: M // 2] = (np.mod(rng.normal(-1.0, 0.05, M // 2) + np.pi, 2 * np.pi) - np.pi).astype(a.dtype)
+    fk = _cplx(int(np.prod(N)), rng, dt)
+    opts = {"msub": msub} if msub else {}
+    c = gpu_transform(2, pts, fk, N, eps, 1, dt, opts)
+    assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, eps, 1)) <= TOL_O2[dt]
