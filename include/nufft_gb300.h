@@ -142,7 +142,8 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *              "bin2" in 3D); it is a spreading method, so a type 2 plan
  *              given it runs as SM (info "method" then reads SM).
  *   "bin1", "bin2", "bin3"   bin size m_i in fine-grid cells (Sec. III-A), >= 1.
- *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1.
+ *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1; at most
+ *              8192 for 3D type 2 plans with the SM interpolator.
  *   "threads"  threads per block of the SM / GM-sort spreading and
  *              interpolation kernels (multiple of 32, 32..1024; lowered to
  *              what a kernel's register use allows).  Default 256, and 512

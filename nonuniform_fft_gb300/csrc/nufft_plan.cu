@@ -460,6 +460,9 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   } else {
     p->msub = p->type == 2 ? 2048 : 1024;
   }
+  // the 3D shared-memory interpolator keeps a per-block order of its points
+  // next to the tile (single precision; the cap applies to both)
+  if (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM && p->msub > 8192) p->msub = 8192;
   // GM packs a point's cell index into int32
   if (p->method == NUFFT_METHOD_GM && nufft::grid_cells(p) >= (int64_t(1) << 31)) return NUFFT_ERR_TOO_LARGE;
   // the cell-level sort indexes (bin, cell) pairs with int32

@@ -400,3 +400,18 @@ def test_interp_clustered_and_ragged(dim, N, dt, eps, msub):
     opts = {"msub": msub} if msub else {}
     c = gpu_transform(2, pts, fk, N, eps, 1, dt, opts)
     assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, eps, 1)) <= TOL_O2[dt]
+
+
+def test_interp3d_large_msub_is_capped():
+    """A 3D type 2 plan asked for huge subproblems interpolates with at most
+    8192 points per subproblem (its per-block point order lives next to the
+    tile in shared memory) and still matches the oracle."""
+    rng = np.random.default_rng(44)
+    N = (16, 20, 12)
+    M = 30000
+    pts = _pts(3, M, "cluster", rng, "f32")
+    fk = _cplx(int(np.prod(N)), rng, "f32")
+    info = {}
+    c = gpu_transform(2, pts, fk, N, 1e-5, 1, "f32", {"msub": 100000}, plan_out=info)
+    assert info["msub"] == 8192
+    assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, 1e-5, 1)) <= TOL_O2["f32"]
