@@ -102,9 +102,6 @@ DF_HD DF df_sum(DF a, DF b) {
   return df_quick(s, e);
 }
 
-// acc += b.
-DF_HD void df_add(DF &acc, DF b) { acc = df_sum(acc, b); }
-
 DF_HD DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
 
 // a / b (b > 0): one correction of the single-precision quotient.

@@ -68,25 +68,6 @@ __global__ void bin_count_kernel(PointsIn a, int32_t *counts, int32_t *bin_of, i
   rank_of[j] = atomicAdd(&counts[bin], 1);
 }
 
-template <typename T>
-__global__ void permute_kernel(PointsIn a, const int32_t *starts, const int32_t *bin_of,
-                               const int32_t *rank_of, int32_t *perm, T *g0, T *g1, T *g2) {
-  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= a.M) return;
-  const int32_t pos = starts[bin_of[j]] + rank_of[j];
-  perm[pos] = (int32_t)j;
-  T *out[3] = {g0, g1, g2};
-  bool bad = false;
-  for (int d = 0; d < a.dim; d++) {
-    double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
-    int cell = (int)floor(g);
-    if (cell >= a.n[d]) cell = a.n[d] - 1;
-    // bin-relative coordinate in [0, m): exact in double, then rounded to T
-    double rel = g - (double)((cell / a.m[d]) * a.m[d]);
-    out[d][pos] = (T)rel;
-  }
-}
-
 __device__ __forceinline__ float below(float v) { return nextafterf(v, 0.0f); }
 __device__ __forceinline__ double below(double v) { return ::nextafter(v, 0.0); }
 
