@@ -458,7 +458,9 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
     const int64_t fill = M / (p->dim <= 2 ? 152 * 32 : 152 * 4);
     p->msub = (int)std::max<int64_t>(64, std::min<int64_t>(cap, fill));
   } else {
-    p->msub = p->type == 2 ? 2048 : 1024;
+    // 3D single-precision interpolation: one subproblem per 16 x 16 x 8 bin at
+    // the bench density, and fuller buckets for its bank-spread point order
+    p->msub = p->type == 2 ? (p->dim == 3 && p->dtype == 0 ? 4096 : 2048) : 1024;
   }
   // the 3D shared-memory interpolator keeps a per-block order of its points
   // next to the tile (single precision; the cap applies to both)
