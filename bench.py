@@ -438,6 +438,8 @@ def run_ours(args, wl):
                        "points_per_step_per_gpu": pts_per_step,
                        "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
                        "msub": info["msub"], "nsub": info["nsub"],
+                       "fine_grid_fft": ("fused pruned passes with the correction" if info["fft"]
+                                         else "cuFFT + correction kernel"),
                        "l2": "flushed between timed steps (256 MiB write, untimed)",
                        "plan_options": opts,
                        "vectors_per_transform": B, "vectors_per_launch": vpp,
@@ -448,7 +450,9 @@ def run_ours(args, wl):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (4 if has2 else 2) * launches * K,
+            # per transform and launch pass: spreading or interpolation plus the
+            # correction kernel, or plus the two fused FFT passes
+            "gpu_launches": (2 if has2 else 1) * (3 if info["fft"] else 2) * launches * K,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

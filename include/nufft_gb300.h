@@ -64,8 +64,9 @@ typedef struct nufft_plan_s *nufft_plan_t;
 /* Indices of nufft_get_timings() output (milliseconds of the last execute /
  * setpts, measured with CUDA events on the plan's stream). */
 #define NUFFT_T_SPREAD_INTERP 0    /* spreading (type 1) or interpolation (type 2) kernel */
-#define NUFFT_T_FFT 1              /* cuFFT execution */
-#define NUFFT_T_DECONV_PAD 2       /* correction + truncation (type 1) or correction + padding (type 2) */
+#define NUFFT_T_FFT 1              /* cuFFT execution; with the fused FFT, its x pass */
+#define NUFFT_T_DECONV_PAD 2       /* correction + truncation (type 1) or correction + padding (type 2);
+                                      with the fused FFT, the y pass that includes them */
 #define NUFFT_T_ZERO 3             /* clearing the fine grid before spreading (type 1) */
 #define NUFFT_T_EXEC 4             /* whole execute on the device (first to last event) */
 #define NUFFT_T_SETPTS 5           /* whole setpts on the device */
@@ -85,7 +86,8 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_I_MSUB 10            /* points per subproblem cap M_sub */
 #define NUFFT_I_METHOD 11          /* spreading method in use (NUFFT_METHOD_*) */
 #define NUFFT_I_BATCH 12           /* vectors per pass of nufft_execute_batch */
-#define NUFFT_I_COUNT 13
+#define NUFFT_I_FFT 13             /* 1: fused pruned FFT in use (option "fft"), 0: cuFFT */
+#define NUFFT_I_COUNT 14
 
 /* Spreading / interpolation methods (option "method"). */
 #define NUFFT_METHOD_AUTO 0
@@ -153,6 +155,12 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *              next execute.
  *   "regtile_cols"  tile columns per lane of the REGTILE spreader: 1, 2 or 4
  *              (0: 1).
+ *   "fft"      0 (default): 2D complex64 plans whose fine grid sizes are
+ *              powers of two from 256 to 4096 take the fine-grid FFT as two
+ *              passes of the library's own kernels, pruned to the modes of
+ *              I_N and fused with the correction of eq. (10) / (11); other
+ *              plans use cuFFT.  1: always cuFFT and the separate correction
+ *              kernels.
  * Errors: BAD_ARG (NULL), BAD_OPT (unknown key or invalid value).
  */
 int nufft_set_opt(nufft_plan_t plan, const char *key, double value);

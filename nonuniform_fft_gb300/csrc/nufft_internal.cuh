@@ -50,6 +50,7 @@ struct nufft_plan_s {
   int opt_threads = 0;         // 0: default
   int opt_regtile_cols = 0;    // 0: default
   int opt_batch = 0;           // vectors per pass of a batched execute (0: default)
+  int opt_fft = 0;             // 0: fused pruned FFT where supported, 1: cuFFT
 
   // --- resolved at setpts ------------------------------------------------
   int method = NUFFT_METHOD_SM;
@@ -63,6 +64,7 @@ struct nufft_plan_s {
   int64_t M = 0;
   bool have_pts = false;
   int nvec = 1;                // vectors in the pass being launched (blockIdx.y range)
+  bool fused_fft = false;      // fine-grid FFT by the fused pruned passes (fft2d_fused.cu)
 
   // --- device memory ----------------------------------------------------
   void *grid = nullptr;            // grid_vecs fine grids, each n1 n2 n3 complex, x fastest
@@ -93,6 +95,9 @@ struct nufft_plan_s {
   int64_t cap_stage_f = 0;
   void *stage_xyz = nullptr;       // staging for host coordinates (3 M reals)
   int64_t cap_stage_xyz = 0;
+  void *fft_tw = nullptr;          // fused FFT: exp(s 2 pi i t / max(n1, n2)), complex64
+  void *fft_work = nullptr;        // fused FFT: N1 x n2 complex per vector of a pass
+  int64_t cap_fft_work = 0;
 
   cufftHandle fft = 0;
   bool fft_made = false;
@@ -100,7 +105,6 @@ struct nufft_plan_s {
 
   // --- timing -------------------------------------------------------------
   cudaEvent_t ev[8] = {};
-  bool ev_made = false;
   bool exec_recorded = false;
   std::vector<cudaEvent_t> xev;   // execute: 5 events per pass
   int xpasses = 0;                 // passes of the last execute
@@ -144,6 +148,18 @@ cudaError_t launch_interp_1d(const nufft_plan_s *p, void *c);
 // deconv.cu: type 1 correction + truncation, type 2 correction + padding.
 cudaError_t launch_deconvolve(const nufft_plan_s *p, void *f);
 cudaError_t launch_pad(const nufft_plan_s *p, const void *f);
+
+// fft2d_fused.cu: the fine-grid FFT of 2D complex64 plans whose fine grid
+// sizes are powers of two in 256..4096, pruned to the kept modes and fused
+// with the correction steps.  Type 1: stage 0 is the x pass (grid ->
+// workspace), stage 1 the y pass with the correction (workspace -> f).
+// Type 2: stage 0 is the correction, padding and y pass (f -> workspace),
+// stage 1 the x pass (workspace -> grid).
+bool fused_fft_supported(const nufft_plan_s *p);
+std::vector<float> fused_fft_twiddles(int64_t len, int sign);  // interleaved re, im
+int64_t fused_fft_work_elems(const nufft_plan_s *p);           // complex per vector
+cudaError_t launch_fused_t1(const nufft_plan_s *p, int stage, void *f);
+cudaError_t launch_fused_t2(const nufft_plan_s *p, int stage, const void *f);
 
 // scan.cu: exclusive prefix sum of n int32 values; out has n + 1 entries and
 // out[n] receives the total.  scratch holds scan_scratch_len(n) ints.

@@ -200,11 +200,13 @@ void release(nufft_plan_s *p) {
   cudaFree(p->stage_c);
   cudaFree(p->stage_f);
   cudaFree(p->stage_xyz);
+  cudaFree(p->fft_tw);
+  cudaFree(p->fft_work);
   if (p->fft_made) cufftDestroy(p->fft);
   for (auto &h : p->fft_many) cufftDestroy(h.second);
   for (auto &e : p->xev) cudaEventDestroy(e);
-  if (p->ev_made)
-    for (auto &e : p->ev) cudaEventDestroy(e);
+  for (auto &e : p->ev)  // also the ones made before a failed makeplan
+    if (e) cudaEventDestroy(e);
 }
 
 int cuda_code(cudaError_t e) {
@@ -342,6 +344,14 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
       if (e != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
     }
     if (rc) break;
+    if (nufft::fused_fft_supported(p)) {
+      const std::vector<float> tw = nufft::fused_fft_twiddles(std::max(p->n[0], p->n[1]), p->iflag);
+      if (cudaMalloc(&p->fft_tw, tw.size() * 4) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
+      if (cudaMemcpy(p->fft_tw, tw.data(), tw.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+        rc = NUFFT_ERR_CUDA;
+        break;
+      }
+    }
     // cuFFT: row-major dims, slowest first (our x index is fastest)
     cufftResult fr;
     const cufftType ft = dtype == 0 ? CUFFT_C2C : CUFFT_Z2Z;
@@ -357,7 +367,6 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
     for (auto &e : p->ev)
       if (cudaEventCreate(&e) != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
     if (rc) break;
-    p->ev_made = true;
   } while (false);
   if (rc) {
     cudaGetLastError();
@@ -387,6 +396,9 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
   } else if (!std::strcmp(key, "batch")) {
     if (v != 0 && (v < 1 || v > 1024 || v != (double)(int)v)) return NUFFT_ERR_BAD_OPT;
     p->opt_batch = (int)v;
+  } else if (!std::strcmp(key, "fft")) {
+    if (v != 0 && v != 1) return NUFFT_ERR_BAD_OPT;
+    p->opt_fft = (int)v;
   } else if (!std::strcmp(key, "regtile_cols")) {
     if (v != 0 && v != 1 && v != 2 && v != 4) return NUFFT_ERR_BAD_OPT;
     p->opt_regtile_cols = (int)v;
@@ -474,6 +486,7 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   // per SM busy
   const int def_threads = (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM) ? 512 : 256;
   p->threads = p->opt_threads > 0 ? p->opt_threads : def_threads;
+  p->fused_fft = p->opt_fft == 0 && p->fft_tw != nullptr;
   p->M = M;
 
   // coordinates in host memory are staged through a device buffer
@@ -541,6 +554,9 @@ int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
     p->grid = g;
     p->grid_vecs = pass;
   }
+  if (p->fused_fft &&
+      (rc = grow_buffer(&p->fft_work, &p->cap_fft_work, (int64_t)(pass * nufft::fused_fft_work_elems(p) * cb))))
+    return rc;
   while ((int64_t)p->xev.size() < npass * kPassEvents) {
     cudaEvent_t e;
     if (cudaEventCreate(&e) != cudaSuccess) return NUFFT_ERR_CUDA;
@@ -559,8 +575,8 @@ int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
       return NUFFT_ERR_CUDA;
     if (p->type == 2 && f_host && cudaMemcpyAsync(df, fu, nv * f_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return NUFFT_ERR_CUDA;
-    cufftHandle plan_fft;
-    if ((rc = fft_plan_for(p, (int)nv, &plan_fft))) return rc;
+    cufftHandle plan_fft = 0;
+    if (!p->fused_fft && (rc = fft_plan_for(p, (int)nv, &plan_fft))) return rc;
     p->nvec = (int)nv;
     cudaEvent_t *ev = &p->xev[k * kPassEvents];
     auto fft = [&]() -> int {
@@ -591,22 +607,27 @@ int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
       return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);
     };
     if (p->type == 1) {
-      // zero -> spread (eq. (7)) -> FFT (eq. (9)) -> correct + truncate (eq. (10))
+      // zero -> spread (eq. (7)) -> FFT (eq. (9)) -> correct + truncate (eq. (10));
+      // fused: x pass, then y pass with the correction
       if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess ||
           (e = cudaMemsetAsync(p->grid, 0, (size_t)(nv * cells) * cb, s)) != cudaSuccess ||
           (e = cudaEventRecord(ev[1], s)) != cudaSuccess || (e = spread()) != cudaSuccess ||
           (e = cudaEventRecord(ev[2], s)) != cudaSuccess)
         break;
-      if ((rc = fft())) break;
-      if ((e = cudaEventRecord(ev[3], s)) != cudaSuccess || (e = nufft::launch_deconvolve(p, df)) != cudaSuccess ||
+      if (p->fused_fft ? (e = nufft::launch_fused_t1(p, 0, df)) != cudaSuccess : (rc = fft()) != NUFFT_OK) break;
+      if ((e = cudaEventRecord(ev[3], s)) != cudaSuccess ||
+          (e = p->fused_fft ? nufft::launch_fused_t1(p, 1, df) : nufft::launch_deconvolve(p, df)) != cudaSuccess ||
           (e = cudaEventRecord(ev[4], s)) != cudaSuccess)
         break;
     } else {
-      // correct + pad (eq. (11)) -> FFT (eq. (12)) -> interpolate (Sec. II-B c)
+      // correct + pad (eq. (11)) -> FFT (eq. (12)) -> interpolate (Sec. II-B c);
+      // fused: correction, padding and y pass, then x pass
       if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess) break;
-      if (p->M > 0 && (e = nufft::launch_pad(p, df)) != cudaSuccess) break;
+      if (p->M > 0 && (e = p->fused_fft ? nufft::launch_fused_t2(p, 0, df) : nufft::launch_pad(p, df)) != cudaSuccess)
+        break;
       if ((e = cudaEventRecord(ev[1], s)) != cudaSuccess) break;
-      if (p->M > 0 && (rc = fft())) break;
+      if (p->M > 0 && (p->fused_fft ? (e = nufft::launch_fused_t2(p, 1, df)) != cudaSuccess : (rc = fft()) != NUFFT_OK))
+        break;
       if ((e = cudaEventRecord(ev[2], s)) != cudaSuccess || (e = interp()) != cudaSuccess ||
           (e = cudaEventRecord(ev[3], s)) != cudaSuccess)
         break;
@@ -666,7 +687,8 @@ int nufft_get_timings(nufft_plan_t p, double *ms, int n) {
 int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
   if (!p || !info || n < 0) return NUFFT_ERR_BAD_ARG;
   const int64_t v[NUFFT_I_COUNT] = {p->w,    p->n[0], p->n[1], p->n[2], p->M,      p->nbins,  p->nsub,
-                                    p->m[0], p->m[1], p->m[2], p->msub, p->method, batch_pass(p)};
+                                    p->m[0], p->m[1], p->m[2], p->msub, p->method, batch_pass(p),
+                                    p->fused_fft ? 1 : 0};
   for (int i = 0; i < n && i < NUFFT_I_COUNT; i++) info[i] = v[i];
   return NUFFT_OK;
 }
