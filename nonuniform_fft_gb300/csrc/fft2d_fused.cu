@@ -149,7 +149,6 @@ __device__ __forceinline__ void fft_stages(float2 *buf, const float2 *__restrict
   for (int g = 0; g < G; g++) {
     const int j = jt + g * TPV;
     const int k = j & (NS - 1);
-#pragma unroll
     {
       // u^r, u = w^{k L/(NS R)}, for r < R from one table read:
       // u^{2m} = (u^m)^2 and u^{2m+1} = u^{m+1} u^m, at most three complex

@@ -104,6 +104,18 @@ __device__ __forceinline__ int es_extended_df(double g, DF beta, DF (&ext)[WX]) 
   return (int)cellf - HW;
 }
 
+// The cell offset xb travels in a spare slot of the staged y weights: as
+// the int's bits in single precision (no conversion on either side), as an
+// exactly representable value in double.
+template <typename T>
+__device__ __forceinline__ T xb_pack(int v);
+template <>
+__device__ __forceinline__ float xb_pack<float>(int v) { return __int_as_float(v); }
+template <>
+__device__ __forceinline__ double xb_pack<double>(int v) { return (double)v; }
+__device__ __forceinline__ int xb_unpack(float v) { return __float_as_int(v); }
+__device__ __forceinline__ int xb_unpack(double v) { return (int)v; }
+
 template <typename T>
 struct RegParams {
   using CT = typename Cplx<T>::type;
@@ -224,7 +236,7 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
           const int xb = es_extended<T, W, G::WXP>(gx[u], a.beta_e, ex);
           es_extended<T, W, G::WXP>(gy[u], a.beta_e, ey);
           if constexpr (G::XB_IN_ROW)
-            ey[G::WX] = T(xb);  // exact: |xb| < 2^24
+            ey[G::WX] = xb_pack<T>(xb);
           else
             st.xb[q] = xb;
 #pragma unroll
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(128) spread_regtile2d_kernel(RegParams<T> a) {
         // [0, W + 2C - 2] for points of this lane's window
         int xbq;
         if constexpr (G::XB_IN_ROW)
-          xbq = (int)wy[G::WX < G::WXP ? G::WX : 0];
+          xbq = xb_unpack(wy[G::WX < G::WXP ? G::WX : 0]);
         else
           xbq = st.xb[q];
         int e0 = x0 - xbq + (C - 1);
