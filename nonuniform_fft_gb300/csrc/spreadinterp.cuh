@@ -354,29 +354,29 @@ __global__ void interp_sm_kernel(SIParams<T> a) {
     }
   }
 
-  // stage the padded bin of the fine grid (periodic wrap) in shared memory;
-  // each thread issues four loads before its four stores
+  // stage the padded bin of the fine grid (periodic wrap) in shared memory:
+  // one warp per tile row, lanes along the row (no division per cell), four
+  // rows' loads in flight per lane before their stores
   {
-    const int cells = p1 * p2 * p3;
-    for (int base = threadIdx.x; base < cells; base += 4 * blockDim.x) {
-      C v[4];
-      int at[4];
+    const int rows = p2 * p3, nw = blockDim.x >> 5, lane = threadIdx.x & 31;
+    for (int r0 = threadIdx.x >> 5; r0 < rows; r0 += 4 * nw) {
+      for (int c = lane; c < p1; c += 32) {
+        const int l1 = wrap_tile(o1 + c, a.n1);
+        C v[4];
 #pragma unroll
-      for (int u = 0; u < 4; u++) {
-        const int t = base + u * (int)blockDim.x;
-        at[u] = t;
-        if (t < cells) {
-          const int s1 = t % p1, r = t / p1;
-          const int s2 = r % p2, s3 = r / p2;
-          const int l1 = wrap_tile(o1 + s1, a.n1);
-          const int l2 = wrap_tile(o2 + s2, a.n2);
-          const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
-          v[u] = a.grid[l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)];
+        for (int u = 0; u < 4; u++) {
+          const int r = r0 + u * nw;
+          if (r < rows) {
+            const int s2 = DIM == 3 ? r % p2 : r, s3 = DIM == 3 ? r / p2 : 0;
+            const int l2 = wrap_tile(o2 + s2, a.n2);
+            const int l3 = DIM == 3 ? wrap_tile(o3 + s3, a.n3) : 0;
+            v[u] = a.grid[l1 + (int64_t)a.n1 * (l2 + (int64_t)a.n2 * l3)];
+          }
         }
-      }
 #pragma unroll
-      for (int u = 0; u < 4; u++)
-        if (at[u] < cells) tile[at[u]] = v[u];
+        for (int u = 0; u < 4; u++)
+          if (r0 + u * nw < rows) tile[(r0 + u * nw) * p1 + c] = v[u];
+      }
     }
   }
   __syncthreads();
