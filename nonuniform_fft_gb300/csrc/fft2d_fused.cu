@@ -206,6 +206,7 @@ __device__ __forceinline__ void fft_vector(float2 *buf, const float2 *__restrict
 struct FusedArgs {
   const float2 *in;       // the pass's source
   float2 *out;            // the pass's destination
+  float2 *grid;           // type 1 x pass: the fine grids it reads and then clears
   const float *p1, *p2;   // correction factors, N1 and N2 entries (increasing k)
   const float2 *tw;       // exp(s 2 pi i t / tw_len), t < tw_len
   int tw_len;
@@ -222,14 +223,16 @@ __device__ __forceinline__ int mode_of(int q, int N, int h, int n) {
   return -1;
 }
 
-// type 1, x pass: KV fine-grid rows -> T[i1][y]
+// type 1, x pass: KV fine-grid rows -> T[i1][y]; afterwards each thread
+// clears the grid cells it read, so the next type 1 execute finds the fine
+// grid zeroed (the clear of step 1 folded into this pass)
 template <int L, int S>
 __global__ void __launch_bounds__(Shape<L>::THREADS, Shape<L>::MIN_BLOCKS) fft_t1_rows_kernel(FusedArgs a) {
   extern __shared__ __align__(16) float2 fft_smem[];
   constexpr int KV = Shape<L>::KV;
   const int v = threadIdx.x % KV, jt = threadIdx.x / KV;
   const int y = blockIdx.x * KV + v;
-  const float2 *row = a.in + blockIdx.y * a.in_stride + (int64_t)y * L;
+  float2 *row = a.grid + blockIdx.y * a.in_stride + (int64_t)y * L;
   float2 *T = a.out + blockIdx.y * a.out_stride;
   auto in = [&](int q) { return row[q]; };
   auto out = [&](int q, float2 val) {
@@ -237,6 +240,12 @@ __global__ void __launch_bounds__(Shape<L>::THREADS, Shape<L>::MIN_BLOCKS) fft_t
     if (i1 >= 0) T[(int64_t)i1 * a.n2 + y] = val;
   };
   fft_vector<L, S>(fft_smem + v * Shape<L>::LP, a.tw, a.tw_len / L, jt, in, out);
+  // the same cells as the first stage's loads (one thread each)
+  constexpr int TPV = Shape<L>::TPV;
+#pragma unroll
+  for (int g = 0; g < (L / 8) / TPV; g++)
+#pragma unroll
+    for (int r = 0; r < 8; r++) row[jt + g * TPV + r * (L / 8)] = make_float2(0.f, 0.f);
 }
 
 // type 1, y pass + correction: KV rows i1 of T -> f[i2][i1] p1(i1) p2(i2)
@@ -342,6 +351,7 @@ cudaError_t run_pass(const nufft_plan_s *p, Pass pass, const void *src, void *ds
   FusedArgs a{};
   a.in = static_cast<const float2 *>(src);
   a.out = static_cast<float2 *>(dst);
+  a.grid = static_cast<float2 *>(p->grid);
   a.p1 = static_cast<const float *>(p->pfac[0]);
   a.p2 = static_cast<const float *>(p->pfac[1]);
   a.tw = static_cast<const float2 *>(p->fft_tw);

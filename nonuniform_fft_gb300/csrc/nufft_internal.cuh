@@ -69,6 +69,7 @@ struct nufft_plan_s {
   // --- device memory ----------------------------------------------------
   void *grid = nullptr;            // grid_vecs fine grids, each n1 n2 n3 complex, x fastest
   int64_t grid_vecs = 0;
+  int64_t grid_zero_vecs = 0;      // leading fine grids known to be all zero (fused FFT clears them)
   void *pfac[3] = {nullptr, nullptr, nullptr};  // correction factors p_i(k), N_i reals
   int32_t *bin_counts = nullptr;   // nbins + 1
   int32_t *bin_starts = nullptr;   // nbins + 1 (last entry: M)
@@ -152,7 +153,8 @@ cudaError_t launch_pad(const nufft_plan_s *p, const void *f);
 // fft2d_fused.cu: the fine-grid FFT of 2D complex64 plans whose fine grid
 // sizes are powers of two in 256..4096, pruned to the kept modes and fused
 // with the correction steps.  Type 1: stage 0 is the x pass (grid ->
-// workspace), stage 1 the y pass with the correction (workspace -> f).
+// workspace; it leaves the pass's fine grids zeroed), stage 1 the y pass with
+// the correction (workspace -> f).
 // Type 2: stage 0 is the correction, padding and y pass (f -> workspace),
 // stage 1 the x pass (workspace -> grid).
 bool fused_fft_supported(const nufft_plan_s *p);

@@ -553,6 +553,7 @@ int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
     cudaFree(p->grid);
     p->grid = g;
     p->grid_vecs = pass;
+    p->grid_zero_vecs = 0;
   }
   if (p->fused_fft &&
       (rc = grow_buffer(&p->fft_work, &p->cap_fft_work, (int64_t)(pass * nufft::fused_fft_work_elems(p) * cb))))
@@ -608,13 +609,17 @@ int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
     };
     if (p->type == 1) {
       // zero -> spread (eq. (7)) -> FFT (eq. (9)) -> correct + truncate (eq. (10));
-      // fused: x pass, then y pass with the correction
+      // fused: x pass, then y pass with the correction.  The fused x pass
+      // leaves the grids it read zeroed, so the clear is skipped after it.
+      const bool zeroed = p->fused_fft && p->grid_zero_vecs >= nv;
+      p->grid_zero_vecs = 0;
       if ((e = cudaEventRecord(ev[0], s)) != cudaSuccess ||
-          (e = cudaMemsetAsync(p->grid, 0, (size_t)(nv * cells) * cb, s)) != cudaSuccess ||
+          (!zeroed && (e = cudaMemsetAsync(p->grid, 0, (size_t)(nv * cells) * cb, s)) != cudaSuccess) ||
           (e = cudaEventRecord(ev[1], s)) != cudaSuccess || (e = spread()) != cudaSuccess ||
           (e = cudaEventRecord(ev[2], s)) != cudaSuccess)
         break;
       if (p->fused_fft ? (e = nufft::launch_fused_t1(p, 0, df)) != cudaSuccess : (rc = fft()) != NUFFT_OK) break;
+      if (p->fused_fft) p->grid_zero_vecs = nv;
       if ((e = cudaEventRecord(ev[3], s)) != cudaSuccess ||
           (e = p->fused_fft ? nufft::launch_fused_t1(p, 1, df) : nufft::launch_deconvolve(p, df)) != cudaSuccess ||
           (e = cudaEventRecord(ev[4], s)) != cudaSuccess)

@@ -133,3 +133,31 @@ def test_fused_not_used_where_unsupported():
     with nf.Plan(1, (128, 128), -1, 1e-9, "complex128") as plan:
         plan.setpts(*xs)
         assert plan.info()["fft"] == 0
+
+
+def test_fused_repeated_executes_on_one_plan():
+    """The fused x pass leaves the fine grids it read zeroed, and the next type
+    1 execute skips the clear: executes on one plan (one vector, a batch of two
+    that grows the plan's grids, one vector, a batch of two) each equal a fresh
+    plan's result."""
+    rng = np.random.default_rng(66)
+    N, M = (128, 256), 6000
+    pts = _pts(M, rng)
+    cs = [_cplx(M, rng) for _ in range(6)]
+    xs = [torch.from_numpy(p).to(DEV) for p in pts]
+    nm = int(np.prod(N))
+    got = []
+    with nf.Plan(1, N, -1, 1e-5, "complex64") as plan:
+        plan.setpts(*xs)
+        assert plan.info()["fft"] == 1
+        for group in ([0], [1, 2], [3], [4, 5]):
+            c = torch.from_numpy(np.concatenate([cs[i] for i in group])).to(DEV)
+            f = torch.zeros(len(group) * nm, dtype=torch.complex64, device=DEV)
+            if len(group) == 1:
+                plan.execute(c, f)
+            else:
+                plan.execute_batch(len(group), c, f)
+            got += list(f.cpu().numpy().reshape(len(group), nm))
+    for i in range(6):
+        ref, _ = _run(1, N, pts, cs[i], 1e-5, -1)
+        assert oracle.rel_l2(got[i], ref) <= 1e-6, i
