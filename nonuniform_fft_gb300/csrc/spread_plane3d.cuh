@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
         es_extended<T, W, G::WXP>(ld_hint(a.g2 + j, pol_stream), a.beta_e, ey);
         es_extended<T, W, G::WXP>(ld_hint(a.g3 + j, pol_stream), a.beta_e, ez);
         if constexpr (G::XB_IN_ROW)
-          ey[G::WX < G::WXP ? G::WX : 0] = T(xb);  // exact: |xb| < 2^24
+          ey[G::WX < G::WXP ? G::WX : 0] = xb_pack<T>(xb);
         else
           s_xbs[q] = xb;
 #pragma unroll
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(Plane3D<T, W, Z, K>::THREADS)
           for (int v = 0; v < G::WXP; v += G::VEC) Vec16<T>::get(&s_wy[q][v], &wy[v]);
           int d;
           if constexpr (G::XB_IN_ROW)
-            d = x_rel - (int)wy[G::WX < G::WXP ? G::WX : 0];
+            d = x_rel - xb_unpack(wy[G::WX < G::WXP ? G::WX : 0]);
           else
             d = x_rel - s_xbs[q];
           d = d < 0 ? 0 : (d > W ? W : d);
