@@ -197,9 +197,11 @@ int nufft_execute(nufft_plan_t plan, void *c, void *f);
  *   f      nvec * prod N_i complex, vector v at f + v prod N_i.
  * Vectors go through the device in passes of "batch" vectors (info
  * NUFFT_I_BATCH): one zeroing / padding pass, one spreading / interpolation
- * launch, one batched cuFFT and one correction launch per pass, over that
- * many fine grids (allocated at the first execute that needs them, kept by
- * the plan).  Host and device pointers as for nufft_execute; host arrays go
+ * launch, one batched cuFFT and one correction launch per pass (with the
+ * fused FFT of option "fft": its two passes instead of the padding, cuFFT
+ * and correction, and no zeroing when the previous pass left the grids
+ * clear), over that many fine grids (allocated at the first execute that
+ * needs them, kept by the plan).  Host and device pointers as for nufft_execute; host arrays go
  * through staging buffers of one pass.  Timings: stage times summed over the
  * passes, NUFFT_T_EXEC from the first pass's start to the last pass's end.
  * Errors: BAD_ARG, NO_POINTS, ALLOC (fine grids, staging), CUDA, CUFFT.
