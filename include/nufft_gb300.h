@@ -64,9 +64,10 @@ typedef struct nufft_plan_s *nufft_plan_t;
 /* Indices of nufft_get_timings() output (milliseconds of the last execute /
  * setpts, measured with CUDA events on the plan's stream). */
 #define NUFFT_T_SPREAD_INTERP 0    /* spreading (type 1) or interpolation (type 2) kernel */
-#define NUFFT_T_FFT 1              /* cuFFT execution; with the fused FFT, its x pass */
+#define NUFFT_T_FFT 1              /* fine-grid FFT: cuFFT execution; with the fused FFT, both of
+                                      its passes (x and y), which include the correction */
 #define NUFFT_T_DECONV_PAD 2       /* correction + truncation (type 1) or correction + padding (type 2);
-                                      with the fused FFT, the y pass that includes them */
+                                      0 with the fused FFT, whose y pass does this work */
 #define NUFFT_T_ZERO 3             /* clearing the fine grid before spreading (type 1) */
 #define NUFFT_T_EXEC 4             /* whole execute on the device (first to last event) */
 #define NUFFT_T_SETPTS 5           /* whole setpts on the device */
@@ -87,7 +88,8 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_I_METHOD 11          /* spreading method in use (NUFFT_METHOD_*) */
 #define NUFFT_I_BATCH 12           /* vectors per pass of nufft_execute_batch */
 #define NUFFT_I_FFT 13             /* 1: fused pruned FFT in use (option "fft"), 0: cuFFT */
-#define NUFFT_I_COUNT 14
+#define NUFFT_I_SMS 14             /* multiprocessors of the plan's device (sizes the default M_sub) */
+#define NUFFT_I_COUNT 15
 
 /* Spreading / interpolation methods (option "method"). */
 #define NUFFT_METHOD_AUTO 0
@@ -242,10 +244,9 @@ int nufft_get_sort(nufft_plan_t plan, int32_t *counts, int32_t *starts, int32_t 
 /*
  * Bin sort without any memory allocation.  The paper has no counterpart: this
  * entry point exists for callers that cannot call cudaMalloc.  Examples are
- * code running while a stream is being captured into a CUDA graph, where
- * allocation calls are not allowed; hosts whose device memory is entirely
- * reserved by their own pool allocator; and real-time loops that must not pay
- * allocation latency or risk out-of-memory in the middle of a run.
+ * hosts whose device memory is entirely reserved by their own pool allocator,
+ * and real-time loops that must not pay allocation latency or risk
+ * out-of-memory in the middle of a run.
  *
  * It computes what nufft_setpts computes for its counts and permutation: each
  * point's fine-grid cell and bin (bins of bins[i] cells, x fastest, smaller at
@@ -263,10 +264,10 @@ int nufft_get_sort(nufft_plan_t plan, int32_t *counts, int32_t *starts, int32_t 
  * Scratch: a fixed 8.3 MB array in the library's device memory, present on
  * every GPU that loads the library until the process exits.  The first call on
  * each device looks up that array's device address (once, with the device
- * current); make that first call before any stream capture.  All calls share
- * the one array: calls that overlap on the GPU (different streams, or several
- * host threads) race and must be serialised by the caller.  The call returns
- * after the sort has finished (it waits for the stream).
+ * current).  All calls share the one array: calls that overlap on the GPU
+ * (different streams, or several host threads) race and must be serialised by
+ * the caller.  The call blocks until the sort has finished: it ends by copying
+ * an error flag to the host and synchronising the stream.
  * Calls no cudaMalloc, cudaFree or allocating library routine.
  * Errors: BAD_ARG, TOO_LARGE (M or the bin count above the limits),
  * BAD_POINTS (a NaN/Inf coordinate), CUDA.

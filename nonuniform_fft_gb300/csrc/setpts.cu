@@ -470,16 +470,21 @@ extern "C" int nufft_binsort_noalloc(int dim, int dtype, int64_t M, const void *
       !counts || (M > 0 && (!x || !y || (dim == 3 && !z) || !perm)))
     return NUFFT_ERR_BAD_ARG;
   PointsIn a;
-  int64_t nbins = 1;
   for (int d = 0; d < 3; d++) {
     const int64_t n = d < dim ? n_fine[d] : 1, m = d < dim ? bins[d] : 1;
     if (n < 1 || m < 1 || n > (int64_t(1) << 30)) return NUFFT_ERR_BAD_ARG;
     a.n[d] = (int)n;
     a.m[d] = (int)(m < n ? m : n);
     a.nb[d] = (int)((n + a.m[d] - 1) / a.m[d]);
+  }
+  if (M > nufft::kNoAllocMaxPoints) return NUFFT_ERR_TOO_LARGE;
+  // bins per dimension can reach 2^30 each: test each factor against the
+  // limit before multiplying, so the product never overflows
+  int64_t nbins = 1;
+  for (int d = 0; d < 3; d++) {
+    if (a.nb[d] > nufft::kNoAllocMaxBins / nbins) return NUFFT_ERR_TOO_LARGE;
     nbins *= a.nb[d];
   }
-  if (M > nufft::kNoAllocMaxPoints || nbins > nufft::kNoAllocMaxBins) return NUFFT_ERR_TOO_LARGE;
   unsigned char *base = nullptr;
   int rc = nufft::noalloc_scratch(&base);
   if (rc) return rc;

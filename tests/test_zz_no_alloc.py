@@ -1,8 +1,8 @@
 """The no-allocation bin sort (nufft_binsort_noalloc) against the plan path.
 
-It is for callers that cannot allocate device memory (during CUDA graph
-capture, under a host-owned memory pool, in real-time loops), so its scratch
-is a fixed array inside the library.  This file is collected last: a failure
+It is for callers that cannot allocate device memory (under a host-owned
+memory pool, in real-time loops), so its scratch is a fixed array inside the
+library.  This file is collected last: a failure
 here leaves every other test already run.  It must pass alone in a fresh
 process and after the other tests (the shared scratch keeps the previous
 call's contents).
@@ -15,7 +15,6 @@ import torch
 
 import nonuniform_fft_gb300 as nf
 
-pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 
 
@@ -60,6 +59,7 @@ def _noalloc_sort(f, dim, dtype_code, xs, n, m, nbins):
     return rc, counts.cpu().numpy(), perm[:M].cpu().numpy()
 
 
+@pytest.mark.gpu
 @pytest.mark.parametrize("dim,N,bins,dt", [(2, (300, 200), (32, 16), "f32"),
                                            (3, (40, 24, 36), (8, 8, 4), "f64")])
 def test_noalloc_binsort_matches_plan_twice(dim, N, bins, dt):
@@ -75,6 +75,7 @@ def test_noalloc_binsort_matches_plan_twice(dim, N, bins, dt):
             np.testing.assert_array_equal(np.sort(perm[lo:lo + cnt]), np.sort(ref["perm"][lo:lo + cnt]))
 
 
+@pytest.mark.gpu
 def test_noalloc_binsort_rejects_sizes_beyond_limit():
     f = _lib()
     x = torch.zeros(16, dtype=torch.float32, device=DEV)
@@ -88,4 +89,18 @@ def test_noalloc_binsort_rejects_sizes_beyond_limit():
     one = (ctypes.c_int64 * 2)(1, 1)
     rc = f(2, 0, 16, x.data_ptr(), x.data_ptr(), None, big, one, counts.data_ptr(),
            counts.data_ptr(), None)
+    assert rc == nf.ERR_TOO_LARGE
+
+
+@pytest.mark.parametrize("n3", [16, 8])
+def test_noalloc_binsort_bin_count_overflow_is_rejected(n3):
+    """Bin counts whose product overflows int64 (2^30 * 2^30 * n3 single-cell
+    bins wraps to 0 or to a negative number) must give TOO_LARGE from the
+    argument checks, which run before any CUDA call, so no GPU is needed."""
+    f = _lib()
+    buf = (ctypes.c_int32 * 16)()
+    ptr = ctypes.addressof(buf)
+    n = (ctypes.c_int64 * 3)(1 << 30, 1 << 30, n3)
+    one = (ctypes.c_int64 * 3)(1, 1, 1)
+    rc = f(3, 0, 16, ptr, ptr, ptr, n, one, ptr, ptr, None)
     assert rc == nf.ERR_TOO_LARGE
