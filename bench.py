@@ -8,9 +8,11 @@ points already bin-sorted (setpts is excluded, as in the metric).  value =
 nonuniform points transformed per second over the whole job: M per transform
 per step per GPU.
 
-Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle (the
-three-step NUFFT in double precision, single thread) on a bounded sample of
-the same workload instead.
+Prints ONE JSON line (rank 0).  On one GPU the line also carries
+"per_workload": the other workloads, a few steps each, with their throughput,
+stage times and per-kernel HBM rooflines.  --impl reference times the CPU
+oracle (the three-step NUFFT in double precision, on every host core) on a
+bounded sample of the same workload instead.
 """
 from __future__ import annotations
 
@@ -50,6 +52,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the other workloads' short measurements (per_workload)")
+    ap.add_argument("--per-workload-steps", type=int, default=5)
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="points per transform in the CPU baseline sample (0: auto)")
     ap.add_argument("--sigma", type=float, default=2.0,
@@ -182,10 +187,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def cpu_sample_points(wl: W.Workload, budget_cells: float = 1.2e8, sigma: float = 2.0) -> int:
-    """Points in a CPU-oracle sample: about budget_cells kernel-weighted grid
-    updates per transform (w^d per point), so that every workload's sample
-    takes seconds, not minutes."""
+# kernel-weighted grid updates (w^d per point and transform) one host thread
+# gets through in about a second of the oracle's plain loops
+CPU_CELLS_PER_THREAD = 1.2e8
+
+
+def cpu_sample_points(wl: W.Workload, budget_cells: float, sigma: float = 2.0) -> int:
+    """Points per transform in a CPU-oracle sample: about budget_cells
+    kernel-weighted grid updates (w^d per point), at most the whole workload."""
     import oracle
     w = oracle.es_params(wl.eps, sigma)[0]
     return int(min(wl.M, max(20000, budget_cells / w ** wl.dim)))
@@ -193,34 +202,39 @@ def cpu_sample_points(wl: W.Workload, budget_cells: float = 1.2e8, sigma: float 
 
 def cpu_oracle_run(wl: W.Workload, sample_M: int, steps: int = 1, sigma: float = 2.0) -> dict:
     """Time the oracle's three-step NUFFT (type 1, plus type 2 when the
-    workload has it) on the first sample_M points of the workload; returns
-    points/s over `steps` repeats."""
+    workload has it) on the first sample_M points of the workload, on every
+    host core it may use; returns points/s over `steps` repeats."""
     import oracle
     sub = wl.scaled(M=sample_M)
     pts, c = W.sample(sub)
     fk = W.coefficients(wl)
     oracle.build()
+    cores = oracle.cpu_threads()
     t0 = time.perf_counter()
     for _ in range(steps):
-        oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1], sigma)
+        oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1], sigma, threads=cores)
         if 2 in wl.types:
-            oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2], sigma)
+            oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2], sigma, threads=cores)
     dt = time.perf_counter() - t0
     per_step = sample_M * len(wl.types)
     types = " + ".join(f"type {t}" for t in wl.types)
-    return {"value": per_step * steps / dt, "unit": "NU points/s", "cores": 1,
+    whole = "all" if sample_M == wl.M else f"{sample_M} of"
+    return {"value": per_step * steps / dt, "unit": "NU points/s", "cores": cores,
             "kind": "oracle", "seconds": dt,
-            "sample": f"{sample_M} of {wl.M} points of {wl.name}, full {'x'.join(map(str, wl.N))} "
-                      f"modes, {types}, x{steps}; sigma {sigma:g}; double precision, one thread"}
+            "sample": f"{whole} {wl.M} points of {wl.name}, full {'x'.join(map(str, wl.N))} "
+                      f"modes, {types}, x{steps}; sigma {sigma:g}; double precision; spreading "
+                      f"and interpolation on {cores} threads (point chunks), numpy FFT"}
 
 
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    import oracle
+    cores = oracle.cpu_threads()
     # bounded: about a minute of CPU work for the whole --steps + --warmup run
-    per_step = args.cpu_sample or max(
-        5000, cpu_sample_points(wl, 1.2e8 / max(1, (args.steps + args.warmup) / 2), args.sigma))
+    per_step = args.cpu_sample or cpu_sample_points(
+        wl, cores * CPU_CELLS_PER_THREAD / max(1, (args.steps + args.warmup) / 2), args.sigma)
     per_step = min(per_step, wl.M)
     if args.warmup:
         cpu_oracle_run(wl, min(per_step, 20000), 1, args.sigma)
@@ -242,28 +256,47 @@ def run_reference(args, wl):
 
 # ------------------------------------------------------------------ GPU arm
 
-def run_ours(args, wl):
+def kernel_names(wl: W.Workload, method1: int, method2: int) -> dict:
+    """Names of the spreading and interpolation kernels the plans launch."""
+    import nonuniform_fft_gb300 as nf
+    df = "_df" if wl.dtype == "f64" else ""
+    regtile = {1: "spread_reg1d" + df + "_kernel", 2: "spread_regtile2d_kernel",
+               3: "spread_plane3d" + df + "_kernel"}[wl.dim]
+    spread = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
+              nf.METHOD_GM: "spread_gmu_kernel", nf.METHOD_REGTILE: regtile}[method1]
+    sm_interp = {1: "interp_sm1d_kernel", 2: "interp_sm_kernel",
+                 3: "interp_sm3d_df_kernel" if wl.dtype == "f64" else "interp_sm3d_bank_kernel"}
+    interp = {nf.METHOD_GM_SORT: "interp_gm_kernel", nf.METHOD_GM: "interp_gmu_kernel"}.get(
+        method2, sm_interp[wl.dim])
+    return {"spread": spread, "interp": interp}
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_PATH) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (measured copy bandwidth)"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
+
+
+def measure(wl, args, dev, stream, opts, steps: int, warmup: int, B: int = 1,
+            host_legs: bool = True, clocks: bool = False) -> dict:
+    """Time `steps` steps (type 1, plus type 2 when the workload has it) of
+    one workload with its points already sorted; L2 flushed between steps.
+    Returns the throughput, per-stage times, per-kernel HBM rooflines and,
+    with host_legs, the end-to-end (host buffers) figure and timing scopes."""
     import torch
-    import torch.distributed as dist
 
     import nonuniform_fft_gb300 as nf
 
     rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    nf.load_library()
-
     cname = "complex64" if wl.dtype == "f32" else "complex128"
     ctorch = getattr(torch, cname)
     pts, c_np = W.sample(wl)
     fk_np = W.coefficients(wl)
-    stream = torch.cuda.Stream(dev)
     N = wl.N
     with torch.cuda.stream(stream):
         xs = [torch.from_numpy(p).to(dev) for p in pts]
-        B = args.batch
         # B vectors: the workload's own, then copies rotated by a phase each
         c_in = torch.from_numpy(c_np).to(dev)
         f_in = torch.from_numpy(fk_np).to(dev)
@@ -275,101 +308,103 @@ def run_ours(args, wl):
         c_out = torch.empty(B * wl.M, dtype=ctorch, device=dev)
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream.synchronize()
-    del pts
-
-    opts = plan_opts(args)
-    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
-                 **opts)
-    p1.setpts(*xs)
-    p1.setpts(*xs)    # the "setpts" scope is this second call: buffers already allocated
-    p2 = None
-    if 2 in wl.types:
-        p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
-                     **opts)
-        p2.setpts(*xs)
-        p2.setpts(*xs)
-    info = p1.info()
-    n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
+    del pts, c_np, fk_np
 
     has2 = 2 in wl.types
-
-    def step():
-        if B == 1:
-            p1.execute(c_in, f_out)
-            if has2:
-                p2.execute(c_out, f_in)
-        else:
-            p1.execute_batch(B, c_in, f_out)
-            if has2:
-                p2.execute_batch(B, c_out, f_in)
-
-    for _ in range(args.warmup):
-        step()
-    stream.synchronize()
-
-    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage = {k: 0.0 for k in ("spread", "fft1", "deconv", "zero", "pad", "fft2", "interp")}
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            with torch.cuda.stream(stream):
-                flush.zero_()                       # evict the inputs from L2 (untimed)
-            ev0[i].record(stream)
-            step()
-            ev1[i].record(stream)
-            t1 = p1.timings()                       # waits for this step's events
-            t2 = p2.timings() if has2 else {k: 0.0 for k in nf.TIMING_KEYS}
-            stage["spread"] += t1["spread_interp"]
-            stage["fft1"] += t1["fft"]
-            stage["deconv"] += t1["deconv_pad"]
-            stage["zero"] += t1["zero"]
-            stage["pad"] += t2["deconv_pad"]
-            stage["fft2"] += t2["fft"]
-            stage["interp"] += t2["spread_interp"]
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    total_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1))
-    t_max = reduce_max(total_ms, dev)
-    pts_per_step = wl.M * len(wl.types) * B
-    value = job_throughput(world, pts_per_step, args.steps, t_max / 1e3)
-
-    # roofline of the dominant kernel (per-launch averages over the timed region)
-    K = args.steps
-    vpp = min(B, info["batch"]) if B > 1 else 1       # vectors one launch processes
-    launches = -(-B // vpp)                           # spread / interp launches per transform
-    algo = algorithmic_bytes(wl, n, vpp)
-    per_launch = {"spread": stage["spread"] / (K * launches)}
-    if has2:
-        per_launch["interp"] = stage["interp"] / (K * launches)
-    dom = max(per_launch, key=per_launch.get)
+    p1 = nf.Plan(1, N, wl.iflag[1], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
+                 **opts)
+    p2 = nf.Plan(2, N, wl.iflag[2], wl.eps, cname, stream=stream.cuda_stream, sigma=args.sigma,
+                 **opts) if has2 else None
     try:
-        with open(PEAKS_PATH) as fh:
-            peak = float(json.load(fh)["hbm_gbs"])
-        peak_source = "MEASURED_PEAKS.json hbm_gbs (measured copy bandwidth)"
-    except (OSError, ValueError, KeyError):
-        peak, peak_source = 6800.0, "fallback 6.8 TB/s (no MEASURED_PEAKS.json)"
-    achieved = algo[dom] / (per_launch[dom] / 1e3) / 1e9
-    spread_kernel = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
-                     nf.METHOD_GM: "spread_gmu_kernel",
-                     nf.METHOD_REGTILE: {1: "spread_reg1d_kernel", 2: "spread_regtile2d_kernel",
-                                         3: "spread_plane3d_kernel"}[wl.dim]}[info["method"]]
-    interp_kernel = {nf.METHOD_GM_SORT: "interp_gm_kernel", nf.METHOD_GM: "interp_gmu_kernel"}.get(
-        p2.info()["method"] if has2 else 0,
-        "interp_sm1d_kernel" if wl.dim == 1 else "interp_sm_kernel")
-    kernel_name = {"spread": spread_kernel, "interp": interp_kernel}[dom]
-    roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak,
-                "traffic": load_traffic(kernel_name, wl.name),
-                "algorithmic_bytes_per_launch": algo[dom], "launch_ms": per_launch[dom],
-                "peak_source": peak_source}
+        for p in (p1, p2):
+            if p is not None:
+                p.setpts(*xs)
+                p.setpts(*xs)   # the "setpts" scope is this second call: buffers allocated
+        info = p1.info()
+        info2 = p2.info() if has2 else None
+        n = [info["n1"], info["n2"], info["n3"]][: wl.dim]
 
-    # end to end through the C ABI with pinned host buffers
-    e2e = None
-    if not args.no_e2e:
+        def step():
+            if B == 1:
+                p1.execute(c_in, f_out)
+                if has2:
+                    p2.execute(c_out, f_in)
+            else:
+                p1.execute_batch(B, c_in, f_out)
+                if has2:
+                    p2.execute_batch(B, c_out, f_in)
+
+        for _ in range(warmup):
+            step()
+        stream.synchronize()
+
+        ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        stage = {k: 0.0 for k in ("spread", "fft1", "deconv", "zero", "pad", "fft2", "interp")}
+        zeros = {k: 0.0 for k in nf.TIMING_KEYS}
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk = ClockSampler(local) if clocks else None
+        if clk:
+            clk.__enter__()
+        try:
+            for i in range(steps):
+                with torch.cuda.stream(stream):
+                    flush.zero_()                       # evict the inputs from L2 (untimed)
+                ev0[i].record(stream)
+                step()
+                ev1[i].record(stream)
+                t1 = p1.timings()                       # waits for this step's events
+                t2 = p2.timings() if has2 else zeros
+                stage["spread"] += t1["spread_interp"]
+                stage["fft1"] += t1["fft"]
+                stage["deconv"] += t1["deconv_pad"]
+                stage["zero"] += t1["zero"]
+                stage["pad"] += t2["deconv_pad"]
+                stage["fft2"] += t2["fft"]
+                stage["interp"] += t2["spread_interp"]
+            torch.cuda.synchronize()
+        finally:
+            if clk:
+                clk.__exit__(None, None, None)
+        if world > 1:
+            dist.barrier()
+        total_ms = sum(a.elapsed_time(b) for a, b in zip(ev0, ev1))
+        t_max = reduce_max(total_ms, dev)
+        pts_per_step = wl.M * len(wl.types) * B
+        value = job_throughput(world, pts_per_step, steps, t_max / 1e3)
+
+        # HBM roofline of the spreading and interpolation kernels (per-launch
+        # averages of their CUDA-event times over the timed region)
+        vpp = min(B, info["batch"]) if B > 1 else 1       # vectors one launch processes
+        launches = -(-B // vpp)                           # spread / interp launches per transform
+        algo = algorithmic_bytes(wl, n, vpp)
+        peak, peak_source = hbm_peak()
+        names = kernel_names(wl, info["method"], info2["method"] if has2 else 0)
+        rooflines = {}
+        for key in (("spread", "interp") if has2 else ("spread",)):
+            ms = stage[key] / (steps * launches)
+            achieved = algo[key] / (ms / 1e3) / 1e9
+            rooflines[key] = {"bound": "hbm", "kernel": names[key], "achieved": achieved,
+                              "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                              "traffic": load_traffic(names[key], wl.name),
+                              "algorithmic_bytes_per_launch": algo[key], "launch_ms": ms,
+                              "peak_source": peak_source}
+        dom = max(rooflines, key=lambda k: rooflines[k]["launch_ms"])
+        out = {"value": value, "t_max_ms": t_max, "total_ms_rank0": total_ms, "stage": stage,
+               "info": info, "n": n, "rooflines": rooflines, "dominant": dom,
+               "pts_per_step": pts_per_step, "vpp": vpp, "launches": launches,
+               "clocks": clk.summary() if clk else None,
+               # per transform and launch pass: spreading or interpolation plus the
+               # correction kernel, or plus the two fused FFT passes
+               "gpu_launches": (2 if has2 else 1) * (3 if info["fft"] else 2) * launches * steps}
+        out["setpts_ms"] = p1.timings()["setpts"] + (p2.timings()["setpts"] if has2 else 0.0)
+        if not host_legs:
+            return out
+
+        # end to end through the C ABI with pinned host buffers
         hc = c_in.cpu().pin_memory()
         hf = f_in.cpu().pin_memory()
         hf_out = torch.empty(B * int(np.prod(N)), dtype=ctorch).pin_memory()
@@ -387,7 +422,7 @@ def run_ours(args, wl):
                     p2.execute_batch(B, hc_out, hf)
 
         host_step()
-        e2e_steps = max(3, min(args.steps, 10))
+        e2e_steps = max(3, min(steps, 10))
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
@@ -396,17 +431,12 @@ def run_ours(args, wl):
         el = reduce_max(time.perf_counter() - t0, dev)
         cb = hc.element_size()
         modes = int(np.prod(N))
-        e2e = {"value": job_throughput(world, pts_per_step, e2e_steps, el), "unit": "NU points/s",
-               "h2d_bytes_per_step": B * (wl.M * cb + (modes * cb if has2 else 0)),
-               "d2h_bytes_per_step": B * (modes * cb + (wl.M * cb if has2 else 0))}
+        out["e2e"] = {"value": job_throughput(world, pts_per_step, e2e_steps, el),
+                      "unit": "NU points/s",
+                      "h2d_bytes_per_step": B * (wl.M * cb + (modes * cb if has2 else 0)),
+                      "d2h_bytes_per_step": B * (modes * cb + (wl.M * cb if has2 else 0))}
 
-    # timing scopes of [cuFINUFFT] Sec. IV-C: "exec" (the step above), "total"
-    # (setpts + exec, on the device) and "total+mem" (host arrays in and out,
-    # setpts and exec, wall clock, synchronous)
-    setpts_ms = p1.timings()["setpts"] + (p2.timings()["setpts"] if has2 else 0.0)
-    scopes = {"exec_ms": t_max / K, "setpts_ms": setpts_ms, "total_ms": t_max / K + setpts_ms,
-              "setpts_note": "device time of a second setpts per plan (buffers allocated)"}
-    if not args.no_e2e:
+        # "total+mem" scope: host arrays in and out, setpts and exec, wall clock
         hx = [x.cpu().pin_memory() for x in xs]
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -415,50 +445,114 @@ def run_ours(args, wl):
             p2.setpts(*hx)
         host_step()
         torch.cuda.synchronize()
-        scopes["total_mem_ms"] = 1e3 * (time.perf_counter() - t0)
+        out["total_mem_ms"] = 1e3 * (time.perf_counter() - t0)
+        return out
+    finally:
+        p1.close()
+        if p2 is not None:
+            p2.close()
+
+
+def stage_summary(r: dict, steps: int) -> dict:
+    return {k: v / steps for k, v in r["stage"].items()}
+
+
+def workload_config(wl, args, r, opts, B, world) -> dict:
+    info = r["info"]
+    return {"workload": wl.name, "dim": wl.dim, "N": list(wl.N), "M": wl.M,
+            "eps": wl.eps, "sigma": args.sigma, "w": info["w"], "fine_grid": r["n"],
+            "dist": wl.dist, "dtype": wl.dtype,
+            "types": " + ".join(f"type {t} (iflag {wl.iflag[t]:+d})" for t in wl.types)
+                     + " per step",
+            "points_per_step_per_gpu": r["pts_per_step"],
+            "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
+            "msub": info["msub"], "nsub": info["nsub"], "sms": info["sms"],
+            "fine_grid_fft": ("fused pruned passes (x and y) with the correction in the y pass; "
+                              "stage fft1/fft2 hold both passes, deconv/pad are 0"
+                              if info["fft"] else "cuFFT + correction kernel"),
+            "l2": "flushed between timed steps (256 MiB write, untimed)",
+            "plan_options": opts,
+            "vectors_per_transform": B, "vectors_per_launch": r["vpp"],
+            "parallelism": f"replicas x{world}"}
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import nonuniform_fft_gb300 as nf
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    nf.load_library()
+    stream = torch.cuda.Stream(dev)
+    opts = plan_opts(args)
+    B = args.batch
+    K = args.steps
+
+    r = measure(wl, args, dev, stream, opts, K, args.warmup, B, host_legs=not args.no_e2e,
+                clocks=True)
+
+    # the other workloads: a few steps each, default options, one GPU only
+    per_workload = None
+    if world == 1 and not args.no_per_workload:
+        per_workload = {}
+        for name, other in W.WORKLOADS.items():
+            if name == wl.name:
+                continue
+            ro = measure(other, args, dev, stream, {}, args.per_workload_steps, 3, 1,
+                         host_legs=False)
+            per_workload[name] = {
+                "value": ro["value"], "unit": "NU points/s",
+                "ms_per_step": ro["t_max_ms"] / args.per_workload_steps,
+                "steps": args.per_workload_steps, "warmup": 3,
+                "stage_ms_per_step": stage_summary(ro, args.per_workload_steps),
+                "setpts_ms": ro["setpts_ms"],
+                "roofline": ro["rooflines"][ro["dominant"]],
+                "rooflines": ro["rooflines"],
+                "gpu_launches": ro["gpu_launches"],
+                "config": workload_config(other, args, ro, {}, 1, world),
+            }
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_run(wl, args.cpu_sample or cpu_sample_points(wl, sigma=args.sigma), 1,
+        import oracle
+        budget = oracle.cpu_threads() * CPU_CELLS_PER_THREAD
+        cpu = cpu_oracle_run(wl, args.cpu_sample or cpu_sample_points(wl, budget, args.sigma), 1,
                              args.sigma)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
     if rank == 0:
-        steps_ms = total_ms / K
+        # timing scopes of [cuFINUFFT] Sec. IV-C: "exec" (the step above), "total"
+        # (setpts + exec, on the device) and "total+mem" (host arrays in and out,
+        # setpts and exec, wall clock, synchronous)
+        scopes = {"exec_ms": r["t_max_ms"] / K, "setpts_ms": r["setpts_ms"],
+                  "total_ms": r["t_max_ms"] / K + r["setpts_ms"],
+                  "setpts_note": "device time of a second setpts per plan (buffers allocated)"}
+        if "total_mem_ms" in r:
+            scopes["total_mem_ms"] = r["total_mem_ms"]
         line = {
-            "metric": METRIC, "value": value, "unit": "NU points/s", "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": t_max / K,
+            "metric": METRIC, "value": r["value"], "unit": "NU points/s", "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": r["t_max_ms"] / K,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "dim": wl.dim, "N": list(wl.N), "M": wl.M,
-                       "eps": wl.eps, "sigma": args.sigma, "w": info["w"], "fine_grid": n,
-                       "dist": wl.dist,
-                       "types": " + ".join(f"type {t} (iflag {wl.iflag[t]:+d})" for t in wl.types)
-                                + " per step",
-                       "points_per_step_per_gpu": pts_per_step,
-                       "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
-                       "msub": info["msub"], "nsub": info["nsub"],
-                       "fine_grid_fft": ("fused pruned passes with the correction" if info["fft"]
-                                         else "cuFFT + correction kernel"),
-                       "l2": "flushed between timed steps (256 MiB write, untimed)",
-                       "plan_options": opts,
-                       "vectors_per_transform": B, "vectors_per_launch": vpp,
-                       "parallelism": f"replicas x{world}"},
-            "stage_ms_per_step": {k: v / K for k, v in stage.items()},
+            "config": workload_config(wl, args, r, opts, B, world),
+            "stage_ms_per_step": stage_summary(r, K),
             "scopes": scopes,
-            "step_ms_rank0": steps_ms,
-            "roofline": roofline,
+            "step_ms_rank0": r["total_ms_rank0"] / K,
+            "roofline": r["rooflines"][r["dominant"]],
+            "rooflines": r["rooflines"],
             "cpu_baseline": cpu,
-            "e2e": e2e,
-            # per transform and launch pass: spreading or interpolation plus the
-            # correction kernel, or plus the two fused FFT passes
-            "gpu_launches": (2 if has2 else 1) * (3 if info["fft"] else 2) * launches * K,
-            "clocks": clk.summary(),
+            "e2e": r.get("e2e"),
+            "gpu_launches": r["gpu_launches"],
+            "clocks": r["clocks"],
+            "per_workload": per_workload,
         }
         print(json.dumps(line), flush=True)
-    p1.close()
-    if p2 is not None:
-        p2.close()
     if world > 1:
         dist.destroy_process_group()
     return 0

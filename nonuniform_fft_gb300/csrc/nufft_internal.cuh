@@ -41,6 +41,7 @@ struct nufft_plan_s {
   int64_t N[3] = {1, 1, 1};
   int64_t n[3] = {1, 1, 1};
   int device = 0;
+  int num_sms = 1;             // multiprocessors of the device (queried at makeplan)
   cudaStream_t stream = nullptr;
 
   // --- options (applied at setpts) --------------------------------------

@@ -324,7 +324,11 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
   p->stream = static_cast<cudaStream_t>(cuda_stream);
   int rc = NUFFT_OK;
   do {
-    if (cudaGetDevice(&p->device) != cudaSuccess) { rc = NUFFT_ERR_CUDA; break; }
+    if (cudaGetDevice(&p->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+      rc = NUFFT_ERR_CUDA;
+      break;
+    }
     const size_t rs = real_size(p);
     if (cudaMalloc(&p->grid, (size_t)cells * 2 * rs) != cudaSuccess) { rc = NUFFT_ERR_ALLOC; break; }
     p->grid_vecs = 1;
@@ -465,9 +469,10 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
     p->msub = p->opt_msub;
   } else if (p->method == NUFFT_METHOD_REGTILE) {
     // a subproblem is one warp (2D) or one block (3D) walking rows in order:
-    // cap it so that small problems still spread over every SM
+    // cap it so that small problems still spread over every SM (32 warps or
+    // 4 blocks per SM)
     const int64_t cap = p->dim <= 2 ? 512 : 8192;
-    const int64_t fill = M / (p->dim <= 2 ? 152 * 32 : 152 * 4);
+    const int64_t fill = M / ((int64_t)p->num_sms * (p->dim <= 2 ? 32 : 4));
     p->msub = (int)std::max<int64_t>(64, std::min<int64_t>(cap, fill));
   } else {
     // 3D single-precision interpolation: one subproblem per 16 x 16 x 8 bin at
@@ -673,10 +678,12 @@ int nufft_get_timings(nufft_plan_t p, double *ms, int n) {
   };
   int rc;
   if (p->exec_recorded) {
-    // stage times summed over the passes of the last execute
+    // stage times summed over the passes of the last execute; the fused FFT's
+    // y pass (which holds the correction) counts as FFT time
     const int last = p->type == 1 ? 4 : 3;
-    const int stage[2][4] = {{NUFFT_T_ZERO, NUFFT_T_SPREAD_INTERP, NUFFT_T_FFT, NUFFT_T_DECONV_PAD},
-                             {NUFFT_T_DECONV_PAD, NUFFT_T_FFT, NUFFT_T_SPREAD_INTERP, -1}};
+    const int cor = p->fused_fft ? NUFFT_T_FFT : NUFFT_T_DECONV_PAD;
+    const int stage[2][4] = {{NUFFT_T_ZERO, NUFFT_T_SPREAD_INTERP, NUFFT_T_FFT, cor},
+                             {cor, NUFFT_T_FFT, NUFFT_T_SPREAD_INTERP, -1}};
     for (int k = 0; k < p->xpasses; k++) {
       cudaEvent_t *ev = &p->xev[k * kPassEvents];
       for (int i = 0; i < last; i++)
@@ -693,7 +700,7 @@ int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
   if (!p || !info || n < 0) return NUFFT_ERR_BAD_ARG;
   const int64_t v[NUFFT_I_COUNT] = {p->w,    p->n[0], p->n[1], p->n[2], p->M,      p->nbins,  p->nsub,
                                     p->m[0], p->m[1], p->m[2], p->msub, p->method, batch_pass(p),
-                                    p->fused_fft ? 1 : 0};
+                                    p->fused_fft ? 1 : 0, p->num_sms};
   for (int i = 0; i < n && i < NUFFT_I_COUNT; i++) info[i] = v[i];
   return NUFFT_OK;
 }

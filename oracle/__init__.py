@@ -120,6 +120,44 @@ def _ptr(a: np.ndarray | None):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def cpu_threads() -> int:
+    """Host threads the oracle uses by default: every core this process may
+    run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _thread_count(units: int, min_per_thread: int, threads: int | None, cap: int = 1 << 30) -> int:
+    n = threads if threads else min(cpu_threads(), max(1, units // max(1, min_per_thread)))
+    return max(1, min(n, cap, max(1, units)))
+
+
+def _run_all(nthreads: int, fn):
+    """fn(0), ..., fn(nthreads - 1), on separate threads when nthreads > 1
+    (the C loops release the GIL while they run)."""
+    if nthreads == 1:
+        fn(0)
+        return
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(nthreads) as ex:
+        list(ex.map(fn, range(nthreads)))
+
+
+def _on_threads(units: int, min_per_thread: int, threads: int | None, fn):
+    """fn(lo, hi) over contiguous chunks of range(units), one per thread."""
+    nthreads = _thread_count(units, min_per_thread, threads)
+    bounds = np.linspace(0, units, nthreads + 1).astype(np.int64)
+
+    def run(i):
+        lo, hi = int(bounds[i]), int(bounds[i + 1])
+        if hi > lo:
+            fn(lo, hi)
+
+    _run_all(nthreads, run)
+
+
 def _f64(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a), dtype=np.float64)
 
@@ -243,7 +281,7 @@ def direct_type1(pts, c, N, iflag: int, modes=None, threads: int | None = None) 
     shape = tuple(len(k) for k in reversed(ks))
     total = int(np.prod(shape))
     M = x.size
-    nthreads = threads or min(os.cpu_count() or 1, max(1, M // 20000))
+    nthreads = _thread_count(M, 20000, threads)
     bounds = np.linspace(0, M, nthreads + 1).astype(np.int64)
     parts = [np.zeros(total, dtype=np.complex128) for _ in range(nthreads)]
     lib = _load()
@@ -271,9 +309,10 @@ def direct_type1(pts, c, N, iflag: int, modes=None, threads: int | None = None) 
     return out.reshape(shape)
 
 
-def direct_type2(pts, f, N, iflag: int, targets=None) -> np.ndarray:
+def direct_type2(pts, f, N, iflag: int, targets=None, threads: int | None = None) -> np.ndarray:
     """c_j = sum_k f_k exp(+-i k.x_j) ([cuFINUFFT] eq. (3)) at the listed
-    targets (user indices; all points when None)."""
+    targets (user indices; all points when None).  The targets are cut into
+    chunks evaluated on separate threads; each target's sum is independent."""
     dim, x, y, z = _coords(pts)
     f = _c128(f).ravel()
     Nn = np.asarray(list(N), dtype=np.int64)
@@ -282,8 +321,13 @@ def direct_type2(pts, f, N, iflag: int, targets=None) -> np.ndarray:
     t = np.arange(x.size, dtype=np.int64) if targets is None else \
         np.ascontiguousarray(np.asarray(targets, dtype=np.int64))
     out = np.zeros(t.size, dtype=np.complex128)
-    _load().oracle_direct_type2(dim, _ptr(Nn), _ptr(x), _ptr(y), _ptr(z), _ptr(f),
-                                int(iflag), t.size, _ptr(t), _ptr(out))
+    lib = _load()
+
+    def run(lo, hi):
+        lib.oracle_direct_type2(dim, _ptr(Nn), _ptr(x), _ptr(y), _ptr(z), _ptr(f),
+                                int(iflag), hi - lo, _ptr(t[lo:]), _ptr(out[lo:]))
+
+    _on_threads(t.size, max(1, (1 << 22) // max(1, f.size)), threads, run)
     return out
 
 
@@ -297,25 +341,54 @@ def plan_params(N, eps: float, sigma: float = 2.0):
     return w, beta, n
 
 
-def spread(pts, c, n, w: int, beta: float) -> np.ndarray:
-    """Type 1 step 1, eq. (7): fine grid b shaped (n3,) n2, n1 (x fastest)."""
+def spread(pts, c, n, w: int, beta: float, threads: int | None = None) -> np.ndarray:
+    """Type 1 step 1, eq. (7): fine grid b shaped (n3,) n2, n1 (x fastest).
+
+    b is a sum over points, so the points are cut into contiguous chunks in
+    user order, each chunk spread by the plain C loop into its own fine grid
+    on its own thread, and the chunk grids are added in double (rounding
+    order differs from one serial loop only in where the partial sums meet).
+    The thread count is capped so the chunk grids take at most about 4 GB."""
     dim, x, y, z = _coords(pts)
     c = _c128(c)
     nn = np.asarray(list(n), dtype=np.int64)
-    b = np.zeros(tuple(reversed(list(n))), dtype=np.complex128)
-    _load().oracle_spread(dim, _ptr(nn), w, beta, x.size, _ptr(x), _ptr(y), _ptr(z),
-                          _ptr(c), _ptr(b))
+    shape = tuple(reversed(list(n)))
+    grid_bytes = 16 * int(np.prod(shape))
+    cap = max(1, (4 << 30) // max(1, grid_bytes))
+    nthreads = _thread_count(x.size, 20000, threads, cap)
+    grids = [np.empty(shape, dtype=np.complex128) for _ in range(nthreads)]
+    bounds = np.linspace(0, x.size, nthreads + 1).astype(np.int64)
+    lib = _load()
+
+    def run(i):
+        lo, hi = int(bounds[i]), int(bounds[i + 1])
+        lib.oracle_spread(dim, _ptr(nn), w, beta, hi - lo, _ptr(x[lo:]),
+                          None if y is None else _ptr(y[lo:]),
+                          None if z is None else _ptr(z[lo:]), _ptr(c[lo:]), _ptr(grids[i]))
+
+    _run_all(nthreads, run)
+    b = grids[0]
+    for g in grids[1:]:
+        b += g
     return b
 
 
-def interp(pts, b, n, w: int, beta: float) -> np.ndarray:
-    """Type 2 step 3 (Sec. II-B c): c_j = sum_l b_l psi_per(l h - x_j)."""
+def interp(pts, b, n, w: int, beta: float, threads: int | None = None) -> np.ndarray:
+    """Type 2 step 3 (Sec. II-B c): c_j = sum_l b_l psi_per(l h - x_j).
+    Each c_j is independent, so contiguous chunks of points run on separate
+    threads of the plain C loop."""
     dim, x, y, z = _coords(pts)
     b = _c128(b)
     nn = np.asarray(list(n), dtype=np.int64)
     c = np.zeros(x.size, dtype=np.complex128)
-    _load().oracle_interp(dim, _ptr(nn), w, beta, x.size, _ptr(x), _ptr(y), _ptr(z),
-                          _ptr(b), _ptr(c))
+    lib = _load()
+
+    def run(lo, hi):
+        lib.oracle_interp(dim, _ptr(nn), w, beta, hi - lo, _ptr(x[lo:]),
+                          None if y is None else _ptr(y[lo:]),
+                          None if z is None else _ptr(z[lo:]), _ptr(b), _ptr(c[lo:]))
+
+    _on_threads(x.size, 20000, threads, run)
     return c
 
 
@@ -339,12 +412,13 @@ def _outer(ps):
     return out
 
 
-def nufft_type1(pts, c, N, eps: float, iflag: int, sigma: float = 2.0) -> np.ndarray:
+def nufft_type1(pts, c, N, eps: float, iflag: int, sigma: float = 2.0,
+                threads: int | None = None) -> np.ndarray:
     """O2 type 1: spread (eq. (7)), FFT (eq. (9)), truncate + correct (eq. (10)).
     Returns f shaped (N3,) N2, N1."""
     N = list(N)
     w, beta, n = plan_params(N, eps, sigma)
-    b = spread(pts, c, n, w, beta)
+    b = spread(pts, c, n, w, beta, threads)
     bhat = _fft(b, iflag)
     idx = [_fine_index(Ni, ni) for Ni, ni in zip(N, n)]
     sub = bhat[np.ix_(*reversed(idx))]
@@ -352,7 +426,8 @@ def nufft_type1(pts, c, N, eps: float, iflag: int, sigma: float = 2.0) -> np.nda
     return p * sub
 
 
-def nufft_type2(pts, f, N, eps: float, iflag: int, sigma: float = 2.0) -> np.ndarray:
+def nufft_type2(pts, f, N, eps: float, iflag: int, sigma: float = 2.0,
+                threads: int | None = None) -> np.ndarray:
     """O2 type 2: pre-correct + zero-pad (eq. (11)), FFT (eq. (12)),
     interpolate (Sec. II-B c).  f shaped (N3,) N2, N1 or flat."""
     N = list(N)
@@ -363,7 +438,7 @@ def nufft_type2(pts, f, N, eps: float, iflag: int, sigma: float = 2.0) -> np.nda
     idx = [_fine_index(Ni, ni) for Ni, ni in zip(N, n)]
     bhat[np.ix_(*reversed(idx))] = p * f
     b = _fft(bhat, iflag)
-    return interp(pts, b, n, w, beta)
+    return interp(pts, b, n, w, beta, threads)
 
 
 # --------------------------------------------------------------------------

@@ -6,9 +6,12 @@ drawn uniformly from I_N (plus k = 0), type 2 at randomly drawn targets, both
 by the direct sums of eq. (1) / (3) of "cuFINUFFT: a load-balanced GPU library
 for general-purpose nonuniform FFTs".  Bound: 2 eps, except the 3D double
 precision eps = 1e-12 workload, where the method itself (the oracle's own
-three-step NUFFT in double precision) reaches about 3 eps, so 4 eps.  The 2D
-and 1D workloads are also compared mode by mode with the oracle's three-step
-NUFFT (1e-5 relative l2 for complex64, 1e-12 for complex128).
+three-step NUFFT in double precision) reaches about 3 eps, so 4 eps.  Every
+workload is also compared over its whole output array (every mode for type 1,
+every point for type 2) with the oracle's three-step NUFFT at the same w, beta
+and fine grid: 1e-5 relative l2 for complex64, 1e-12 for complex128.  The
+oracle runs on all host cores, which keeps the 3D workloads (3.2e7 points at
+w = 7, 1e7 points at w = 13) to tens of seconds each.
 """
 import numpy as np
 import pytest
@@ -22,6 +25,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 BOUND = {"2d_t1_f32_N64_M1e4": 2, "2d_f32_N1024_M1e7": 2, "2d_t1_f32_N1024_M1e7_cluster": 2,
          "3d_f32_N128_M3.2e7": 2, "3d_f64_N64_M1e7_mix": 4, "1d_f64_N1e6_M1e7": 2}
+TOL_O2 = {"f32": 1e-5, "f64": 1e-12}
 
 
 def _run(wl, t, pts, data):
@@ -58,9 +62,9 @@ def test_type1_full_size(name):
     got = f[np.ix_(*[k + n // 2 for k, n in zip(reversed(ks), reversed(wl.N))])]
     err = oracle.rel_l2(got, ref)
     assert err <= BOUND[name] * wl.eps, f"{name}: type 1 vs direct sum {err:.3e}"
-    if wl.dim <= 2:
-        o2 = oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1])
-        assert oracle.rel_l2(f, o2) <= (1e-5 if wl.dtype == "f32" else 1e-12)
+    o2 = oracle.nufft_type1(pts, c, wl.N, wl.eps, wl.iflag[1])
+    e2 = oracle.rel_l2(f, o2)
+    assert e2 <= TOL_O2[wl.dtype], f"{name}: type 1 vs the oracle's NUFFT {e2:.3e}"
 
 
 @pytest.mark.parametrize("name", [n for n, w in W.WORKLOADS.items() if 2 in w.types])
@@ -74,6 +78,6 @@ def test_type2_full_size(name):
     ref = oracle.direct_type2(pts, fk, wl.N, wl.iflag[2], targets=tg)
     err = oracle.rel_l2(c[tg], ref)
     assert err <= BOUND[name] * wl.eps, f"{name}: type 2 vs direct sum {err:.3e}"
-    if wl.dim <= 2:
-        o2 = oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2])
-        assert oracle.rel_l2(c, o2) <= (1e-5 if wl.dtype == "f32" else 1e-12)
+    o2 = oracle.nufft_type2(pts, fk, wl.N, wl.eps, wl.iflag[2])
+    e2 = oracle.rel_l2(c, o2)
+    assert e2 <= TOL_O2[wl.dtype], f"{name}: type 2 vs the oracle's NUFFT {e2:.3e}"

@@ -220,6 +220,27 @@ def test_nufft_error_close_to_eps(dim, N, M, eps):
             assert e1 >= eps / 4 and e2 >= eps / 4
 
 
+@pytest.mark.parametrize("dim,N,M", [(1, (48,), 3001), (2, (40, 32), 3001), (3, (16, 12, 20), 2003)])
+@pytest.mark.parametrize("eps", [1e-6, 1e-12])
+def test_nufft_threaded_chunks_close_to_eps(dim, N, M, eps):
+    """The oracle spreads and interpolates contiguous chunks of points on
+    separate threads (spread: one fine grid per chunk, summed).  With an odd
+    point count split three ways, a chunk offset or a dropped partial grid
+    would miss the direct sums by far more than eps; the threaded result must
+    stay within [eps/4, 4 eps] of eq. (1) / (3) like the one-thread one."""
+    rng = np.random.default_rng(8)
+    pts = [rng.uniform(-np.pi, np.pi, M) for _ in range(dim)]
+    c = rng.standard_normal(M) + 1j * rng.standard_normal(M)
+    f = rng.standard_normal(int(np.prod(N))) + 1j * rng.standard_normal(int(np.prod(N)))
+    e1 = oracle.rel_l2(oracle.nufft_type1(pts, c, N, eps, -1, threads=3),
+                       oracle.direct_type1(pts, c, N, -1))
+    e2 = oracle.rel_l2(oracle.nufft_type2(pts, f, N, eps, 1, threads=3),
+                       oracle.direct_type2(pts, f, N, 1, threads=3))
+    assert e1 <= 4 * eps and e2 <= 4 * eps
+    if eps >= 1e-11:
+        assert e1 >= eps / 4 and e2 >= eps / 4
+
+
 def test_sigma_rule_is_eq6_at_two():
     """The sigma < 2 reading reduces to eq. (6) itself at sigma = 2."""
     for tol in (0.5, 1e-2, 1e-3, 5e-4, 1e-5, 1e-6, 1e-9, 1e-12, 1e-15):
