@@ -14,6 +14,7 @@
 // multiply-add): g = n * frac(x / (2 pi)), node l at l h (eq. (7)).
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "nufft_internal.cuh"
 
@@ -26,6 +27,8 @@ struct PointsIn {
   int dim;
   int is_double;
   double inv_two_pi;
+  float turn3[3];  // inv_two_pi split exactly into three floats (fold_fast)
+  int fast;        // 1: turn3 is exact, so fold_fast may be used
   int n[3];
   int m[3];
   int nb[3];
@@ -47,6 +50,63 @@ __device__ __forceinline__ double grid_coord(double x, double inv_two_pi, int n,
   double g = __dmul_rn(t, (double)n);
   if (g >= (double)n) g = __dsub_rn(g, (double)n);
   return g;
+}
+
+// Sum of two floats as an unevaluated pair hi + lo, exactly (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float *hi, float *lo) {
+  const float s = a + b;
+  const float bv = s - a;
+  *lo = (a - (s - bv)) + (b - bv);
+  *hi = s;
+}
+
+// The fold of a single-precision coordinate without FP64 arithmetic: g ~
+// n frac(x inv_two_pi) as gh + gl, from exact float products of x with the
+// three-float split of the double inv_two_pi (x c0 and x c1 each as a
+// product and its fused-multiply-add error; x c2 rounded; the fraction of
+// the leading product as a TwoSum pair).  The result is within
+// n (2.5e-14 |x c| + 9e-15) of the double fold grid_coord computes
+// (its own two roundings included), so when gh + gl lies farther than twice
+// that from every integer, floor(g) -- the cell -- is the same as the double
+// fold's.  Returns false, for the caller to take the double fold, when x is
+// not finite, |x| > 1024, n >= 2^24, or g is that close to a cell boundary
+// (about 1e-8 of the coordinates at n = 2048).  Otherwise sets the cell and
+// gh + gl (no part of the integer result depends on gl beyond the check).
+__device__ __forceinline__ bool fold_fast(float x, const float (&c)[3], int n, int *cell, float *gh,
+                                          float *gl) {
+  if (!(fabsf(x) <= 1024.0f) || n >= (1 << 24)) return false;
+  const float p0 = x * c[0], e0 = fmaf(x, c[0], -p0);
+  const float p1 = x * c[1], e1 = fmaf(x, c[1], -p1);
+  const float p2 = x * c[2];
+  float f, fl;
+  two_sum(p0, -floorf(p0), &f, &fl);  // p0 - floor(p0) = f + fl exactly (f in [0, 1])
+  const float tail = ((e0 + p1) + (e1 + p2)) + fl;
+  float s, sl;
+  two_sum(f, tail, &s, &sl);  // frac(x c) up to an integer
+  if (s < 0.0f) {
+    float t, tl;
+    two_sum(s, 1.0f, &t, &tl);
+    s = t;
+    sl += tl;
+  } else if (s >= 1.0f) {
+    float t, tl;
+    two_sum(s, -1.0f, &t, &tl);
+    s = t;
+    sl += tl;
+  }
+  const float nf = (float)n;
+  const float h = s * nf;
+  const float l = fmaf(s, nf, -h) + sl * nf;
+  const float r = rintf(h);
+  const float d = (h - r) + l;  // h - r is exact
+  const float delta = nf * (fabsf(p0) + 1.0f) * 5.6843419e-14f;  // n (|x c| + 1) 2^-44
+  if (fabsf(d) <= delta) return false;
+  const int k = (int)r - (d < 0.0f ? 1 : 0);
+  if (k < 0 || k >= n) return false;
+  *cell = k;
+  *gh = h;
+  *gl = l;
+  return true;
 }
 
 template <typename T>
@@ -88,17 +148,30 @@ __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, 
   bool bad = false;
   int bin = 0, stride = 1, local = 0, lstride = 1;
   for (int d = 0; d < a.dim; d++) {
-    double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
-    int cell = (int)floor(g);
-    if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
+    int cell = 0;
+    T v = T(0);
+    bool done = false;
+    if constexpr (std::is_same<T, float>::value) {
+      float gh, gl;
+      if (a.fast && fold_fast(static_cast<const float *>(a.x[d])[j], a.turn3, a.n[d], &cell, &gh, &gl)) {
+        v = (gh - (float)((cell / a.m[d]) * a.m[d])) + gl;  // the difference is exact
+        done = true;
+      }
+    }
+    if (!done) {
+      const double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
+      cell = (int)floor(g);
+      if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
+      v = (T)(g - (double)((cell / a.m[d]) * a.m[d]));  // exact in double, then rounded to T
+    }
     const int b = cell / a.m[d];
     const int cell_rel = cell - b * a.m[d];
     bin += b * stride;
     stride *= a.nb[d];
     local += cell_rel * lstride;
     lstride *= a.m[d];
-    T v = (T)(g - (double)(b * a.m[d]));  // exact in double, then rounded to T
     if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
+    if (v < (T)cell_rel) v = (T)cell_rel;
     out[d][j] = v;
   }
   if (bad) atomicOr(flag, 1);
@@ -191,6 +264,21 @@ __global__ void sub_fill_kernel(const int32_t *counts, const int32_t *starts,
   table[s] = e;
 }
 
+// inv_two_pi = c0 + c1 + c2 exactly: c0 its nearest float, c1 the nearest
+// float to the (exact) remainder, c2 the rest, which has at most 53 - 48
+// significant bits and so is a float too.
+void split_turn(PointsIn &a) {
+  const double c = a.inv_two_pi;
+  const float c0 = (float)c;
+  const double r = c - (double)c0;
+  const float c1 = (float)r;
+  const float c2 = (float)(r - (double)c1);
+  a.turn3[0] = c0;
+  a.turn3[1] = c1;
+  a.turn3[2] = c2;
+  a.fast = ((double)c0 + (double)c1) + (double)c2 == c;
+}
+
 template <typename Tptr>
 cudaError_t grow(Tptr **ptr, int64_t *cap, int64_t need, size_t elem) {
   if (need <= *cap && *ptr) return cudaSuccess;
@@ -272,6 +360,7 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
   a.dim = p->dim;
   a.is_double = p->dtype;
   a.inv_two_pi = 1.0 / (2.0 * 3.14159265358979323846);
+  split_turn(a);
   for (int d = 0; d < 3; d++) {
     a.n[d] = (int)p->n[d];
     a.m[d] = p->m[d];

@@ -91,6 +91,7 @@ SORT_CASES = [
     (2, (100, 70), 20000, "uniform", "f32", {"msub": 256}),
     (2, (100, 70), 20000, "cluster", "f32", {"msub": 100}),
     (2, (64, 64), 5000, "wild", "f64", {}),
+    (2, (64, 64), 5000, "wild", "f32", {}),
     (3, (20, 24, 36), 30000, "uniform", "f32", {"bin1": 8, "bin2": 8, "bin3": 4, "msub": 128}),
     (3, (20, 24, 36), 30000, "cluster", "f64", {}),
     (2, (3, 5), 50, "uniform", "f32", {"bin1": 5, "bin2": 7}),
@@ -114,6 +115,39 @@ def test_setpts_integer_results_match_oracle(dim, N, M, dist, dt, opts):
     np.testing.assert_array_equal(got["counts"], ref["counts"])
     np.testing.assert_array_equal(got["starts"], ref["starts"])
     np.testing.assert_array_equal(got["subproblems"], ref["subproblems"])
+    for lo, cnt in zip(ref["starts"], ref["counts"]):
+        np.testing.assert_array_equal(np.sort(got["perm"][lo:lo + cnt]), ref["perm"][lo:lo + cnt])
+
+
+def _boundary_coords(n, rng, count):
+    """float32 coordinates at and next to the floats nearest the cell
+    boundaries 2 pi k / n, one period either side too, in random order."""
+    k = rng.integers(0, n + 1, count).astype(np.float64)
+    shift = rng.choice([0.0, -2 * np.pi, 2 * np.pi], count)
+    b = (2 * np.pi * k / n + shift).astype(np.float32)
+    step = rng.integers(-2, 3, count)
+    for s in (1, 2):
+        b = np.where(step >= s, np.nextafter(b, np.float32(np.inf)), b)
+        b = np.where(step <= -s, np.nextafter(b, np.float32(-np.inf)), b)
+    return b
+
+
+@pytest.mark.parametrize("N", [(100, 70), (64, 128)])
+def test_setpts_cells_at_boundaries_match_oracle(N):
+    """Single-cell bins make each point's bin its fine-grid cell: with every
+    coordinate at (or next to) the float nearest a cell boundary, the cells
+    setpts assigns must be the oracle's double-precision fold's."""
+    rng = np.random.default_rng(5)
+    M = 60000
+    with nf.Plan(1, N, -1, 1e-6, "complex64", method=nf.METHOD_SM, bin1=1, bin2=1) as plan:
+        n = [plan.info()["n1"], plan.info()["n2"]]
+        pts = [_boundary_coords(nd, rng, M) for nd in n]
+        plan.setpts(*[torch.from_numpy(p).to(DEV) for p in pts])
+        info = plan.info()
+        got = plan.sort()
+    assert info["bin1"] == 1 and info["bin2"] == 1
+    ref = oracle.binsort(pts, n, [1, 1], info["msub"])
+    np.testing.assert_array_equal(got["counts"], ref["counts"])
     for lo, cnt in zip(ref["starts"], ref["counts"]):
         np.testing.assert_array_equal(np.sort(got["perm"][lo:lo + cnt]), ref["perm"][lo:lo + cnt])
 
