@@ -139,15 +139,13 @@ __device__ __forceinline__ double below(double v) { return ::nextafter(v, 0.0); 
 // coordinate, rounded to T but never up to the next cell (floor stays the
 // point's cell), is written in the caller's order to rel_d and later gathered
 // into sorted order.
+// Key and bin-relative coordinates of point j (see cell_count_kernel).
 template <typename T>
-__global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, int32_t *rank_of,
-                                  int *flag, T *rel0, T *rel1, T *rel2) {
-  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= a.M) return;
-  T *out[3] = {rel0, rel1, rel2};
-  bool bad = false;
+__device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T *const (&out)[3], bool *bad) {
   int bin = 0, stride = 1, local = 0, lstride = 1;
-  for (int d = 0; d < a.dim; d++) {
+#pragma unroll
+  for (int d = 0; d < 3; d++) {
+    if (d >= a.dim) break;
     int cell = 0;
     T v = T(0);
     bool done = false;
@@ -159,7 +157,7 @@ __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, 
       }
     }
     if (!done) {
-      const double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], &bad);
+      const double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], bad);
       cell = (int)floor(g);
       if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
       v = (T)(g - (double)((cell / a.m[d]) * a.m[d]));  // exact in double, then rounded to T
@@ -174,31 +172,99 @@ __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, 
     if (v < (T)cell_rel) v = (T)cell_rel;
     out[d][j] = v;
   }
-  if (bad) atomicOr(flag, 1);
-  const int32_t key = bin * lstride + local;
-  key_of[j] = key;
-  rank_of[j] = atomicAdd(&counts[key], 1);
+  return bin * lstride + local;
 }
 
-// Sorted slot of each point: the one scattered store of the sort.
+// Cell-level key of a point: its bin, then its cell inside the bin (x fastest).
+// Sorting by this key orders the points bin by bin (as Sec. III-A) and, inside
+// each bin, cell by cell, so a bin's points of one fine-grid row (and one x
+// range of that row) form a contiguous run.
+// The fold to the fine grid is done once, here: the point's bin-relative
+// coordinate, rounded to T but never up to the next cell (floor stays the
+// point's cell), is written in the caller's order to rel_d and later gathered
+// into sorted order.  Each thread takes PPT points blockDim.x apart and
+// issues their counter increments back to back, so that several returning
+// atomics are in flight per thread.
+template <typename T, int PPT>
+__global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, int32_t *rank_of,
+                                  int *flag, T *rel0, T *rel1, T *rel2) {
+  const int64_t j0 = (int64_t)blockIdx.x * blockDim.x * PPT + threadIdx.x;
+  T *const out[3] = {rel0, rel1, rel2};
+  bool bad = false;
+  int32_t key[PPT];
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    const int64_t j = j0 + (int64_t)u * blockDim.x;
+    key[u] = j < a.M ? cell_key<T>(a, j, out, &bad) : 0;
+  }
+  int32_t rank[PPT];
+#pragma unroll
+  for (int u = 0; u < PPT; u++)
+    if (j0 + (int64_t)u * blockDim.x < a.M) rank[u] = atomicAdd(&counts[key[u]], 1);
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    const int64_t j = j0 + (int64_t)u * blockDim.x;
+    if (j < a.M) {
+      key_of[j] = key[u];
+      rank_of[j] = rank[u];
+    }
+  }
+  if (bad) atomicOr(flag, 1);
+}
+
+// Sorted slot of each point: the one scattered store of the sort.  PPT
+// points per thread, blockDim.x apart, with their loads issued together.
+template <int PPT>
 __global__ void cell_scatter_kernel(int64_t M, const int32_t *starts, const int32_t *key_of,
                                     const int32_t *rank_of, int32_t *perm) {
-  const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= M) return;
-  perm[starts[key_of[j]] + rank_of[j]] = (int32_t)j;
+  const int64_t j0 = (int64_t)blockIdx.x * blockDim.x * PPT + threadIdx.x;
+  int32_t key[PPT], rank[PPT], slot[PPT];
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    const int64_t j = j0 + (int64_t)u * blockDim.x;
+    key[u] = j < M ? key_of[j] : 0;
+    rank[u] = j < M ? rank_of[j] : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < PPT; u++) slot[u] = j0 + (int64_t)u * blockDim.x < M ? starts[key[u]] + rank[u] : 0;
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    const int64_t j = j0 + (int64_t)u * blockDim.x;
+    if (j < M) perm[slot[u]] = (int32_t)j;
+  }
 }
 
 // Bin-relative coordinates in sorted order: coalesced writes, reads gathered
-// through the permutation (the caller-order arrays stay in L2).
-template <typename T>
+// through the permutation (the caller-order arrays stay in L2).  PPT slots
+// per thread, blockDim.x apart.
+template <typename T, int PPT>
 __global__ void gather_coords_kernel(int64_t M, int dim, const int32_t *perm, const T *rel0,
                                      const T *rel1, const T *rel2, T *g0, T *g1, T *g2) {
-  const int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (q >= M) return;
-  const int32_t j = perm[q];
-  g0[q] = rel0[j];
-  if (dim >= 2) g1[q] = rel1[j];
-  if (dim == 3) g2[q] = rel2[j];
+  const int64_t q0 = (int64_t)blockIdx.x * blockDim.x * PPT + threadIdx.x;
+  int32_t src[PPT];
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    const int64_t q = q0 + (int64_t)u * blockDim.x;
+    src[u] = q < M ? perm[q] : 0;
+  }
+  T v0[PPT], v1[PPT], v2[PPT];
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    if (q0 + (int64_t)u * blockDim.x < M) {
+      v0[u] = rel0[src[u]];
+      v1[u] = dim >= 2 ? rel1[src[u]] : T(0);
+      v2[u] = dim == 3 ? rel2[src[u]] : T(0);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < PPT; u++) {
+    const int64_t q = q0 + (int64_t)u * blockDim.x;
+    if (q < M) {
+      g0[q] = v0[u];
+      if (dim >= 2) g1[q] = v1[u];
+      if (dim == 3) g2[q] = v2[u];
+    }
+  }
 }
 
 // Bin counts and starts from the cell starts (cpb cells per bin).
@@ -375,12 +441,14 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
   for (int d = 0; d < 3; d++)
     rel[d] = static_cast<char *>(p->gtmp) + (size_t)(d < p->dim ? d : 0) * (size_t)M * rs;
   if (M > 0) {
+    constexpr int kPPT = 4;
+    const unsigned blocks_cc = (unsigned)((M + threads * kPPT - 1) / (threads * kPPT));
     if (p->dtype == 0)
-      cell_count_kernel<float><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag,
-                                                             (float *)rel[0], (float *)rel[1], (float *)rel[2]);
+      cell_count_kernel<float, kPPT><<<blocks_cc, threads, 0, s>>>(
+          a, p->cell_counts, p->bin_of, p->rank_of, p->flag, (float *)rel[0], (float *)rel[1], (float *)rel[2]);
     else
-      cell_count_kernel<double><<<blocks_pts, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag,
-                                                              (double *)rel[0], (double *)rel[1], (double *)rel[2]);
+      cell_count_kernel<double, kPPT><<<blocks_cc, threads, 0, s>>>(
+          a, p->cell_counts, p->bin_of, p->rank_of, p->flag, (double *)rel[0], (double *)rel[1], (double *)rel[2]);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
@@ -394,14 +462,16 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
 
   // --- 3. permutation and sorted coordinates ------------------------------
   if (M > 0) {
-    cell_scatter_kernel<<<blocks_pts, threads, 0, s>>>(M, p->cell_starts, p->bin_of, p->rank_of, p->perm);
+    constexpr int kPPT = 4;
+    const unsigned blocks_ppt = (unsigned)((M + threads * kPPT - 1) / (threads * kPPT));
+    cell_scatter_kernel<kPPT><<<blocks_ppt, threads, 0, s>>>(M, p->cell_starts, p->bin_of, p->rank_of, p->perm);
     void *g1 = p->dim >= 2 ? p->gcoord[1] : p->gcoord[0], *g2 = p->dim == 3 ? p->gcoord[2] : p->gcoord[0];
     if (p->dtype == 0)
-      gather_coords_kernel<float><<<blocks_pts, threads, 0, s>>>(
+      gather_coords_kernel<float, kPPT><<<blocks_ppt, threads, 0, s>>>(
           M, p->dim, p->perm, (const float *)rel[0], (const float *)rel[1], (const float *)rel[2],
           (float *)p->gcoord[0], (float *)g1, (float *)g2);
     else
-      gather_coords_kernel<double><<<blocks_pts, threads, 0, s>>>(
+      gather_coords_kernel<double, kPPT><<<blocks_ppt, threads, 0, s>>>(
           M, p->dim, p->perm, (const double *)rel[0], (const double *)rel[1], (const double *)rel[2],
           (double *)p->gcoord[0], (double *)g1, (double *)g2);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
