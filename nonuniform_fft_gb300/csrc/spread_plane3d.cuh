@@ -45,13 +45,16 @@ struct Plane3D {
   static constexpr int WXP = (WX + VEC - 1) / VEC * VEC;
   static constexpr int WYS = (WXP / VEC) % 2 == 0 ? WXP + VEC : WXP;
   static constexpr int WCS = WX | 1;        // odd row stride of the c * x-weight products
+  // odd row stride of the z weights: the lanes of a warp read one column of
+  // different points' rows, which an even stride folds onto a few banks
+  static constexpr int WZS = WX | 1;
   static constexpr int M1 = 32 - 2 * PAD;   // bin width (x)
   static constexpr int P3 = K * Z;          // padded-bin planes
   static constexpr int M3 = P3 - 2 * PAD;   // bin depth (z)
   static constexpr int THREADS = 32 * K;
   // staged points per batch within STAGE_KB of dynamic shared memory (three
   // blocks of 8 warps share an SM); larger batches mean fewer block barriers
-  static constexpr int PT_BYTES = (int)sizeof(T) * (WYS + WX + 2 * WCS) + (XB_IN_ROW ? 0 : 4);
+  static constexpr int PT_BYTES = (int)sizeof(T) * (WYS + WZS + 2 * WCS) + (XB_IN_ROW ? 0 : 4);
   static constexpr int S_FIT = (STAGE_KB * 1024 / PT_BYTES) / 32 * 32;
   static constexpr int S = S_FIT < 1024 ? S_FIT : 1024;
   static_assert(S >= 32, "staging buffer too small");
@@ -63,7 +66,7 @@ struct __align__(16) Plane3DStage {
   using G = Plane3D<T, W, Z, K>;
   typename Cplx<T>::type cwx[G::S][G::WCS];
   T wy[G::S][G::WYS];
-  T wz[G::S][G::WX];
+  T wz[G::S][G::WZS];
   int xb[G::XB_IN_ROW ? 1 : G::S];
 };
 
