@@ -49,12 +49,16 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS) + ["all"])
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the other workloads' short measurements (per_workload)")
     ap.add_argument("--per-workload-steps", type=int, default=5)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the spreading / interpolation kernel over a grid of plan options "
+                         "(bins, M_sub, columns per lane, threads) for --workload, or for every "
+                         "workload with --workload all; one JSON line per option set")
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="points per transform in the CPU baseline sample (0: auto)")
     ap.add_argument("--sigma", type=float, default=2.0,
@@ -558,8 +562,95 @@ def run_ours(args, wl):
     return 0
 
 
+# ------------------------------------------------------------------ option sweep
+
+# Option sets swept per workload and transform type (plan options of
+# nufft_set_opt; {} is the library's default).  Type 1 plans use the
+# register-tile spreader, type 2 plans the shared-memory interpolator.
+def sweep_space(wl: W.Workload, t: int) -> list:
+    def grid(**axes):
+        out = [{}]
+        for k, vals in axes.items():
+            out = [dict(o, **{k: v}) for o in out for v in vals]
+        return out
+    if wl.dim == 2 and t == 1:
+        return [{}] + grid(regtile_cols=[1, 2], bin2=[32, 64, 128], msub=[256, 512, 1024, 2048])
+    if wl.dim == 2 and t == 2:
+        return [{}] + [dict(o, bin2=o["bin1"]) for o in
+                       grid(bin1=[16, 26, 32, 48], msub=[1024, 2048, 4096], threads=[128, 256, 512])]
+    if wl.dim == 3 and t == 1:
+        return [{}] + grid(bin2=[4, 8, 16, 32], msub=[2048, 4096, 8192])
+    if wl.dim == 3 and t == 2:
+        return [{}] + grid(msub=[2048, 4096, 8192], threads=[256, 512, 1024])
+    if wl.dim == 1 and t == 1:
+        return [{}] + grid(msub=[128, 256, 512, 1024, 2048])
+    return [{}] + grid(bin1=[256, 512, 1024, 2048], msub=[512, 1024, 2048, 4096])
+
+
+def run_sweep(args):
+    import torch
+
+    import nonuniform_fft_gb300 as nf
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    nf.load_library()
+    stream = torch.cuda.Stream(dev)
+    names = sorted(W.WORKLOADS) if args.workload == "all" else [args.workload]
+    best = {}
+    for name in names:
+        wl = W.WORKLOADS[name]
+        cname = "complex64" if wl.dtype == "f32" else "complex128"
+        ctorch = getattr(torch, cname)
+        pts, c_np = W.sample(wl)
+        with torch.cuda.stream(stream):
+            xs = [torch.from_numpy(p).to(dev) for p in pts]
+            c_in = torch.from_numpy(c_np).to(dev)
+            f_in = torch.from_numpy(W.coefficients(wl)).to(dev)
+            f_out = torch.empty(int(np.prod(wl.N)), dtype=ctorch, device=dev)
+            c_out = torch.empty(wl.M, dtype=ctorch, device=dev)
+            flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        stream.synchronize()
+        steps = 3 if wl.dim == 3 and wl.dtype == "f64" else 6
+        for t in wl.types:
+            for opts in sweep_space(wl, t):
+                try:
+                    plan = nf.Plan(t, wl.N, wl.iflag[t], wl.eps, cname, stream=stream.cuda_stream, **opts)
+                    plan.setpts(*xs)
+                except nf.NufftError as e:      # an option set the kernel cannot take
+                    print(json.dumps({"sweep": name, "type": t, "opts": opts, "error": str(e)}), flush=True)
+                    continue
+                info = plan.info()
+                ms = []
+                for i in range(2 + steps):
+                    with torch.cuda.stream(stream):
+                        flush.zero_()
+                    if t == 1:
+                        plan.execute(c_in, f_out)
+                    else:
+                        plan.execute(c_out, f_in)
+                    if i >= 2:
+                        ms.append(plan.timings()["spread_interp"])
+                plan.close()
+                rec = {"sweep": name, "type": t, "opts": opts, "ms_median": statistics.median(ms),
+                       "ms_min": min(ms), "bins": [info["bin1"], info["bin2"], info["bin3"]][: wl.dim],
+                       "msub": info["msub"], "nsub": info["nsub"]}
+                print(json.dumps(rec), flush=True)
+                key = (name, t)
+                if key not in best or rec["ms_median"] < best[key]["ms_median"]:
+                    best[key] = rec
+        del xs, c_in, f_in, f_out, c_out, flush
+        torch.cuda.empty_cache()
+    for (name, t), rec in sorted(best.items()):
+        print(json.dumps({"sweep_best": name, "type": t, "opts": rec["opts"],
+                          "ms_median": rec["ms_median"]}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.sweep:
+        return run_sweep(args)
     wl = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)

@@ -143,15 +143,17 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *              AUTO picks REGTILE for type 1 and SM for type 2 (the only
  *              methods in 1D; others give BAD_OPT there).  REGTILE
  *              fixes the bin size (the "bin" options are ignored, except
- *              "bin2" in 3D); it is a spreading method, so a type 2 plan
- *              given it runs as SM (info "method" then reads SM).
+ *              "bin2", the bin height, in 2D and 3D); it is a spreading
+ *              method, so a type 2 plan given it runs as SM (info "method"
+ *              then reads SM).
  *   "bin1", "bin2", "bin3"   bin size m_i in fine-grid cells (Sec. III-A), >= 1.
  *   "msub"     cap M_sub on points per subproblem (SM step 1), >= 1; at most
  *              8192 for 3D type 2 plans with the SM interpolator.
  *   "threads"  threads per block of the SM / GM-sort spreading and
  *              interpolation kernels (multiple of 32, 32..1024; lowered to
- *              what a kernel's register use allows).  Default 256, and 512
- *              for the 3D shared-memory interpolators.
+ *              what a kernel's register use allows).  Default 256; for the
+ *              3D shared-memory interpolators 512 (complex64) and 1024
+ *              (complex128).
  *   "batch"    vectors per pass of nufft_execute_batch, 1..1024 (0: as many
  *              fine grids as fit in 1 GiB, at most 64).  Takes effect at the
  *              next execute.

@@ -440,12 +440,14 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   if (p->dim == 1) {
     // one padded-bin column per lane for spreading; long bins for the
     // interpolator's staged tile, short enough in single precision that the
-    // bin-relative coordinate keeps ~1e-6 cell resolution
-    m[0] = p->type == 1 ? 32 - 2 * ((p->w + 1) / 2) : (p->dtype == 0 ? 128 : 1024);
+    // bin-relative coordinate keeps ~1e-6 cell resolution (double: 512 cells,
+    // from the option sweep of the 1D double-precision workload)
+    m[0] = p->type == 1 ? 32 - 2 * ((p->w + 1) / 2) : (p->dtype == 0 ? 128 : 512);
     if (p->opt_bin[0] > 0 && p->type == 2) m[0] = p->opt_bin[0];
   } else if (p->method == NUFFT_METHOD_REGTILE) {
     if (p->dim == 2) {
       nufft::regtile2d_bins(p->w, p->regtile_cols, &m[0], &m[1]);
+      if (p->opt_bin[1] > 0) m[1] = p->opt_bin[1];  // rows are free
     } else {
       nufft::plane3d_bins(p->w, p->dtype, &m[0], &m[1], &m[2]);
       if (p->opt_bin[1] > 0) m[1] = p->opt_bin[1];  // rows are free
@@ -470,14 +472,17 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   } else if (p->method == NUFFT_METHOD_REGTILE) {
     // a subproblem is one warp (2D) or one block (3D) walking rows in order:
     // cap it so that small problems still spread over every SM (32 warps or
-    // 4 blocks per SM)
-    const int64_t cap = p->dim <= 2 ? 512 : 8192;
+    // 4 blocks per SM).  Caps from the option sweeps: 512 points in 2D, 8192
+    // in 3D single precision, 2048 for the two-float 3D spreader
+    const int64_t cap = p->dim <= 2 ? 512 : (p->dtype == 0 ? 8192 : 2048);
     const int64_t fill = M / ((int64_t)p->num_sms * (p->dim <= 2 ? 32 : 4));
     p->msub = (int)std::max<int64_t>(64, std::min<int64_t>(cap, fill));
   } else {
-    // 3D single-precision interpolation: one subproblem per 16 x 16 x 8 bin at
-    // the bench density, and fuller buckets for its bank-spread point order
-    p->msub = p->type == 2 ? (p->dim == 3 && p->dtype == 0 ? 4096 : 2048) : 1024;
+    // interpolation: 4096 points in 3D (single precision: one subproblem per
+    // 16 x 16 x 8 bin at the bench density, fuller buckets for its
+    // bank-spread point order) and for the long 1D double-precision bins,
+    // 2048 otherwise (option sweeps)
+    p->msub = p->type == 2 ? (p->dim == 3 || (p->dim == 1 && p->dtype == 1) ? 4096 : 2048) : 1024;
   }
   // the 3D shared-memory interpolator keeps a per-block order of its points
   // next to the tile (single precision; the cap applies to both)
@@ -488,8 +493,10 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
   // the 3D interpolators hold one large tile per block (two blocks per SM in
   // single precision, one in double): more threads per block keep more warps
-  // per SM busy
-  const int def_threads = (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM) ? 512 : 256;
+  // per SM busy (512 and 1024 from the option sweeps)
+  const int def_threads = (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM)
+                              ? (p->dtype == 0 ? 512 : 1024)
+                              : 256;
   p->threads = p->opt_threads > 0 ? p->opt_threads : def_threads;
   p->fused_fft = p->opt_fft == 0 && p->fft_tw != nullptr;
   p->M = M;

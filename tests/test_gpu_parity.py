@@ -166,15 +166,19 @@ METHODS = [nf.METHOD_SM, nf.METHOD_GM_SORT, nf.METHOD_REGTILE, nf.METHOD_GM]
 
 @pytest.mark.parametrize("cols", [1, 2, 4])
 @pytest.mark.parametrize("dt,eps", [("f32", 1e-2), ("f32", 1e-6), ("f64", 1e-9), ("f64", 1e-12)])
-def test_regtile_columns_per_lane(cols, dt, eps):
-    """The register-tile spreader with 1, 2 and 4 tile columns per lane, on a
-    grid whose width is not a multiple of the bin width (ragged last bin)."""
+@pytest.mark.parametrize("rows", [0, 13, 128])
+def test_regtile_columns_per_lane(cols, dt, eps, rows):
+    """The register-tile spreader with 1, 2 and 4 tile columns per lane and
+    bin heights of 13, 64 (default) and 128 rows, on a grid whose sizes are
+    not multiples of the bin (ragged last bins)."""
     rng = np.random.default_rng(31)
     N = (150, 90)
     M = 30000
     pts = _pts(2, M, "uniform", rng, dt)
     c = _cplx(M, rng, dt)
     opts = {"method": nf.METHOD_REGTILE, "regtile_cols": cols, "msub": 700}
+    if rows:
+        opts["bin2"] = rows
     f = gpu_transform(1, pts, c, N, eps, -1, dt, opts)
     assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, -1)) <= TOL_O2[dt]
 
