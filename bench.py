@@ -123,6 +123,26 @@ def algorithmic_bytes(wl: W.Workload, n, nvec: int = 1) -> dict:
     }
 
 
+# ALU roofline of the spreading and interpolation kernels: each point adds
+# (or gathers) w^d complex values times a real weight, 2 w^d real
+# multiply-adds.  Peaks from the unit counts and clocks: FP32, 128 FMA lanes
+# per SM x 152 SMs x 2.07 GHz; FP64, the nominal 1.25 TFLOP/s of this part
+# (the double-precision kernels run two-float arithmetic on the FP32 pipes,
+# so they are measured against the FP64 rate they stand in for).
+FP32_TFMA = 128 * 152 * 2.07e9 / 1e12
+FP64_TFMA = 1.25 / 2
+
+
+def alu_roofline(wl: W.Workload, w: int, launch_ms: float, vpp: int = 1) -> dict:
+    fma = 2.0 * w ** wl.dim * wl.M * vpp
+    achieved = fma / (launch_ms / 1e3) / 1e12
+    peak = FP32_TFMA if wl.dtype == "f32" else FP64_TFMA
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFMA/s",
+            "frac": achieved / peak, "algorithmic_fma_per_launch": fma,
+            "peak_source": ("FP32: 128 lanes x 152 SMs x 2.07 GHz" if wl.dtype == "f32"
+                            else "FP64: nominal 1.25 TFLOP/s (two-float kernels on the FP32 pipes)")}
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -395,7 +415,8 @@ def measure(wl, args, dev, stream, opts, steps: int, warmup: int, B: int = 1,
                               "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                               "traffic": load_traffic(names[key], wl.name),
                               "algorithmic_bytes_per_launch": algo[key], "launch_ms": ms,
-                              "peak_source": peak_source}
+                              "peak_source": peak_source,
+                              "alu": alu_roofline(wl, info["w"], ms, vpp)}
         dom = max(rooflines, key=lambda k: rooflines[k]["launch_ms"])
         out = {"value": value, "t_max_ms": t_max, "total_ms_rank0": total_ms, "stage": stage,
                "info": info, "n": n, "rooflines": rooflines, "dominant": dom,
