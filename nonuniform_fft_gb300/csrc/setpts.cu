@@ -436,7 +436,6 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
       cudaMemsetAsync(p->flag, 0, sizeof(int), s) != cudaSuccess)
     return NUFFT_ERR_CUDA;
   const int threads = 256;
-  const unsigned blocks_pts = (unsigned)((M + threads - 1) / threads);
   void *rel[3];
   for (int d = 0; d < 3; d++)
     rel[d] = static_cast<char *>(p->gtmp) + (size_t)(d < p->dim ? d : 0) * (size_t)M * rs;
