@@ -280,12 +280,12 @@ def run_reference(args, wl):
 
 # ------------------------------------------------------------------ GPU arm
 
-def kernel_names(wl: W.Workload, method1: int, method2: int) -> dict:
+def kernel_names(wl: W.Workload, method1: int, method2: int, tile3d: int = 1) -> dict:
     """Names of the spreading and interpolation kernels the plans launch."""
     import nonuniform_fft_gb300 as nf
     df = "_df" if wl.dtype == "f64" else ""
     regtile = {1: "spread_reg1d" + df + "_kernel", 2: "spread_regtile2d_kernel",
-               3: "spread_plane3d" + df + "_kernel"}[wl.dim]
+               3: "spread_slab3d_kernel" if tile3d == 2 else "spread_plane3d" + df + "_kernel"}[wl.dim]
     spread = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
               nf.METHOD_GM: "spread_gmu_kernel", nf.METHOD_REGTILE: regtile}[method1]
     sm_interp = {1: "interp_sm1d_kernel", 2: "interp_sm_kernel",
@@ -406,7 +406,7 @@ def measure(wl, args, dev, stream, opts, steps: int, warmup: int, B: int = 1,
         launches = -(-B // vpp)                           # spread / interp launches per transform
         algo = algorithmic_bytes(wl, n, vpp)
         peak, peak_source = hbm_peak()
-        names = kernel_names(wl, info["method"], info2["method"] if has2 else 0)
+        names = kernel_names(wl, info["method"], info2["method"] if has2 else 0, info.get("tile3d", 1))
         rooflines = {}
         for key in (("spread", "interp") if has2 else ("spread",)):
             ms = stage[key] / (steps * launches)

@@ -89,7 +89,8 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_I_BATCH 12           /* vectors per pass of nufft_execute_batch */
 #define NUFFT_I_FFT 13             /* 1: fused pruned FFT in use (option "fft"), 0: cuFFT */
 #define NUFFT_I_SMS 14             /* multiprocessors of the plan's device (sizes the default M_sub) */
-#define NUFFT_I_COUNT 15
+#define NUFFT_I_TILE3D 15          /* 3D REGTILE spreader in use: 1 planes per warp, 2 slab bins (0: not 3D) */
+#define NUFFT_I_COUNT 16
 
 /* Spreading / interpolation methods (option "method"). */
 #define NUFFT_METHOD_AUTO 0
@@ -159,6 +160,13 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *              next execute.
  *   "regtile_cols"  tile columns per lane of the REGTILE spreader: 1, 2 or 4
  *              (0: 1).
+ *   "tile3d"   3D REGTILE spreader: 1, one block per subproblem, each warp
+ *              holding two padded planes of a bin of 32 - 2 ceil(w/2) x 8 x
+ *              (16 - 2 ceil(w/2)) cells (16 x 4 x ... in double precision);
+ *              2, one warp per subproblem holding all w+1 planes of a bin one
+ *              cell thick in z (32 - 2 ceil(w/2) x 32 x 1 cells; complex64 and
+ *              w <= 8 only, else BAD_OPT at setpts).  0 (default): 2 where it
+ *              applies, else 1.
  *   "fft"      0 (default): 2D complex64 plans whose fine grid sizes are
  *              powers of two from 256 to 4096 take the fine-grid FFT as two
  *              passes of the library's own kernels, pruned to the modes of

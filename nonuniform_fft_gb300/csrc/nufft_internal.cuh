@@ -52,6 +52,7 @@ struct nufft_plan_s {
   int opt_regtile_cols = 0;    // 0: default
   int opt_batch = 0;           // vectors per pass of a batched execute (0: default)
   int opt_fft = 0;             // 0: fused pruned FFT where supported, 1: cuFFT
+  int opt_tile3d = 0;          // 3D register-tile spreader: 0 auto, 1 planes per warp, 2 slab bins
 
   // --- resolved at setpts ------------------------------------------------
   int method = NUFFT_METHOD_SM;
@@ -60,6 +61,7 @@ struct nufft_plan_s {
   int msub = 1024;
   int threads = 256;
   int regtile_cols = 4;        // tile columns per lane of the register-tile spreader
+  int tile3d = 1;              // 3D register-tile spreader in use: 1 planes per warp, 2 slab bins
   int64_t nbins = 0;
   int64_t nsub = 0;
   int64_t M = 0;
@@ -142,6 +144,12 @@ void regtile2d_bins(int w, int cols, int *m1, int *m2);
 template <typename T>
 cudaError_t launch_spread_plane3d(const nufft_plan_s *p, const void *c);
 void plane3d_bins(int w, int dtype, int *m1, int *m2, int *m3);
+// 3D single-precision spreader with one-cell-thick bins (spread_slab3d.cuh),
+// for widths up to kSlab3DMaxWidth ((w+1)^2 complex accumulators per lane).
+constexpr int kSlab3DMaxWidth = 8;
+bool slab3d_supported(int w, int dtype);
+void slab3d_bins(int w, int *m1, int *m2, int *m3);
+cudaError_t launch_spread_slab3d(const nufft_plan_s *p, const void *c);
 
 // spreadinterp_1d.cu: 1D register-tile spreading and shared-memory interpolation.
 cudaError_t launch_spread_1d(const nufft_plan_s *p, const void *c);

@@ -183,6 +183,56 @@ def test_regtile_columns_per_lane(cols, dt, eps, rows):
     assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, -1)) <= TOL_O2[dt]
 
 
+@pytest.mark.parametrize("eps", [1e-2, 1e-5, 1e-6, 1e-7])
+@pytest.mark.parametrize("N,dist,opts", [((20, 24, 36), "uniform", {}),
+                                         ((33, 18, 16), "cluster", {}),
+                                         ((20, 24, 36), "uniform", {"msub": 37, "bin2": 5})])
+def test_slab3d_spreader(eps, N, dist, opts):
+    """The 3D single-precision spreader with one-cell-thick bins (option
+    tile3d = 2; widths 3, 6, 7 and 8 here), ragged grids, clustered points
+    and short subproblems, against the oracle's three-step NUFFT."""
+    rng = np.random.default_rng(41)
+    M = 40000
+    pts = _pts(3, M, dist, rng, "f32")
+    c = _cplx(M, rng, "f32")
+    info = {}
+    f = gpu_transform(1, pts, c, N, eps, -1, "f32",
+                      dict(opts, method=nf.METHOD_REGTILE, tile3d=2), plan_out=info)
+    assert info["bin3"] == 1
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, -1)) <= TOL_O2["f32"]
+
+
+@pytest.mark.parametrize("eps", [1e-3, 1e-6])
+@pytest.mark.parametrize("dist", ["uniform", "cluster"])
+def test_plane3d_spreader_single_precision(eps, dist):
+    """The 3D single-precision spreader with planes per warp (option tile3d =
+    1; the default where slab bins do not apply, w > 8)."""
+    rng = np.random.default_rng(43)
+    N = (20, 24, 36)
+    M = 40000
+    pts = _pts(3, M, dist, rng, "f32")
+    c = _cplx(M, rng, "f32")
+    info = {}
+    f = gpu_transform(1, pts, c, N, eps, -1, "f32", {"method": nf.METHOD_REGTILE, "tile3d": 1},
+                      plan_out=info)
+    assert info["tile3d"] == 1 and info["bin3"] > 1
+    assert oracle.rel_l2(f, oracle.nufft_type1(pts, c, N, eps, -1)) <= TOL_O2["f32"]
+
+
+def test_slab3d_rejects_unsupported():
+    """Slab bins are built for single precision and widths up to 8."""
+    x = torch.zeros(10, dtype=torch.float64, device=DEV)
+    with nf.Plan(1, (8, 8, 8), -1, 1e-9, "complex128", method=nf.METHOD_REGTILE, tile3d=2) as plan:
+        with pytest.raises(nf.NufftError) as e:
+            plan.setpts(x, x, x)
+        assert e.value.code == nf.ERR_BAD_OPT
+    xf = torch.zeros(10, dtype=torch.float32, device=DEV)
+    with nf.Plan(1, (8, 8, 8), -1, 1e-9, "complex64", method=nf.METHOD_REGTILE, tile3d=2) as plan:
+        with pytest.raises(nf.NufftError) as e:      # w = 10
+            plan.setpts(xf, xf, xf)
+        assert e.value.code == nf.ERR_BAD_OPT
+
+
 @pytest.mark.parametrize("method", METHODS)
 @pytest.mark.parametrize("dim,N,dt,eps", T_CASES)
 def test_type1_matches_oracle(dim, N, dt, eps, method):
