@@ -41,6 +41,10 @@ struct Slab3D {
   static constexpr int M1 = 32 - 2 * PAD;   // bin width (x)
   static constexpr int S = 64;              // staged points per batch
   static constexpr int WARPS = 4;
+  // blocks per SM the registers are sized for: 3 up to w = 7 (at w = 7 the
+  // cap of 168 registers spills 20 bytes and takes the 3D bench spread from
+  // 4.87 to 4.38 ms; 4 blocks, 128 registers, spill far more: 9.8 ms)
+  static constexpr int MIN_BLOCKS = W <= 7 ? 3 : 2;
 };
 
 template <int W>
@@ -68,7 +72,8 @@ struct Slab3DParams {
 };
 
 template <int W>
-__global__ void __launch_bounds__(32 * Slab3D<W>::WARPS) spread_slab3d_kernel(Slab3DParams a) {
+__global__ void __launch_bounds__(32 * Slab3D<W>::WARPS, Slab3D<W>::MIN_BLOCKS)
+    spread_slab3d_kernel(Slab3DParams a) {
   using G = Slab3D<W>;
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
