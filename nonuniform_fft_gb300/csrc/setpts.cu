@@ -139,13 +139,54 @@ __device__ __forceinline__ double below(double v) { return ::nextafter(v, 0.0); 
 // coordinate, rounded to T but never up to the next cell (floor stays the
 // point's cell), is written in the caller's order to rel_d and later gathered
 // into sorted order.
+// A point's bin-relative coordinates as one record of setpts' scratch: DIM
+// values, padded to 4 in 3D, so that gathering a point's record through the
+// permutation touches one 32-byte sector (not one per dimension).
+template <typename T, int DIM>
+struct CoordRec {
+  static constexpr int PACK = DIM == 3 ? 4 : DIM;
+  static __device__ __forceinline__ void store(T *rec, const T (&v)[DIM]) {
+    if constexpr (DIM == 1) {
+      rec[0] = v[0];
+    } else if constexpr (DIM == 2) {
+      using V2 = typename std::conditional<std::is_same<T, float>::value, float2, double2>::type;
+      *reinterpret_cast<V2 *>(rec) = V2{v[0], v[1]};
+    } else if constexpr (std::is_same<T, float>::value) {
+      *reinterpret_cast<float4 *>(rec) = make_float4(v[0], v[1], v[2], 0.f);
+    } else {
+      reinterpret_cast<double2 *>(rec)[0] = make_double2(v[0], v[1]);
+      reinterpret_cast<double2 *>(rec)[1] = make_double2(v[2], 0.0);
+    }
+  }
+  static __device__ __forceinline__ void load(const T *rec, T (&v)[DIM]) {
+    if constexpr (DIM == 1) {
+      v[0] = rec[0];
+    } else if constexpr (DIM == 2) {
+      using V2 = typename std::conditional<std::is_same<T, float>::value, float2, double2>::type;
+      const V2 t = *reinterpret_cast<const V2 *>(rec);
+      v[0] = t.x;
+      v[1] = t.y;
+    } else if constexpr (std::is_same<T, float>::value) {
+      const float4 t = *reinterpret_cast<const float4 *>(rec);
+      v[0] = t.x;
+      v[1] = t.y;
+      v[2] = t.z;
+    } else {
+      const double2 t0 = reinterpret_cast<const double2 *>(rec)[0];
+      const double2 t1 = reinterpret_cast<const double2 *>(rec)[1];
+      v[0] = t0.x;
+      v[1] = t0.y;
+      v[2] = t1.x;
+    }
+  }
+};
+
 // Key and bin-relative coordinates of point j (see cell_count_kernel).
-template <typename T>
-__device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T *const (&out)[3], bool *bad) {
+template <typename T, int DIM>
+__device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T (&out)[DIM], bool *bad) {
   int bin = 0, stride = 1, local = 0, lstride = 1;
 #pragma unroll
-  for (int d = 0; d < 3; d++) {
-    if (d >= a.dim) break;
+  for (int d = 0; d < DIM; d++) {
     int cell = 0;
     T v = T(0);
     bool done = false;
@@ -170,7 +211,7 @@ __device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T *con
     lstride *= a.m[d];
     if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
     if (v < (T)cell_rel) v = (T)cell_rel;
-    out[d][j] = v;
+    out[d] = v;
   }
   return bin * lstride + local;
 }
@@ -181,21 +222,26 @@ __device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T *con
 // range of that row) form a contiguous run.
 // The fold to the fine grid is done once, here: the point's bin-relative
 // coordinate, rounded to T but never up to the next cell (floor stays the
-// point's cell), is written in the caller's order to rel_d and later gathered
-// into sorted order.  Each thread takes PPT points blockDim.x apart and
-// issues their counter increments back to back, so that several returning
-// atomics are in flight per thread.
-template <typename T, int PPT>
+// point's cell), is written in the caller's order, one record per point
+// (CoordRec), and later gathered into sorted order.  Each thread takes PPT
+// points blockDim.x apart and issues their counter increments back to back,
+// so that several returning atomics are in flight per thread.
+template <typename T, int DIM, int PPT>
 __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, int32_t *rank_of,
-                                  int *flag, T *rel0, T *rel1, T *rel2) {
+                                  int *flag, T *rel) {
+  using R = CoordRec<T, DIM>;
   const int64_t j0 = (int64_t)blockIdx.x * blockDim.x * PPT + threadIdx.x;
-  T *const out[3] = {rel0, rel1, rel2};
   bool bad = false;
   int32_t key[PPT];
 #pragma unroll
   for (int u = 0; u < PPT; u++) {
     const int64_t j = j0 + (int64_t)u * blockDim.x;
-    key[u] = j < a.M ? cell_key<T>(a, j, out, &bad) : 0;
+    key[u] = 0;
+    if (j < a.M) {
+      T v[DIM];
+      key[u] = cell_key<T, DIM>(a, j, v, &bad);
+      R::store(rel + j * R::PACK, v);
+    }
   }
   int32_t rank[PPT];
 #pragma unroll
@@ -234,12 +280,12 @@ __global__ void cell_scatter_kernel(int64_t M, const int32_t *starts, const int3
   }
 }
 
-// Bin-relative coordinates in sorted order: coalesced writes, reads gathered
-// through the permutation (the caller-order arrays stay in L2).  PPT slots
-// per thread, blockDim.x apart.
-template <typename T, int PPT>
-__global__ void gather_coords_kernel(int64_t M, int dim, const int32_t *perm, const T *rel0,
-                                     const T *rel1, const T *rel2, T *g0, T *g1, T *g2) {
+// Bin-relative coordinates in sorted order: coalesced writes, one record per
+// point gathered through the permutation.  PPT slots per thread, blockDim.x
+// apart.
+template <typename T, int DIM, int PPT>
+__global__ void gather_coords_kernel(int64_t M, const int32_t *perm, const T *rel, T *g0, T *g1, T *g2) {
+  using R = CoordRec<T, DIM>;
   const int64_t q0 = (int64_t)blockIdx.x * blockDim.x * PPT + threadIdx.x;
   int32_t src[PPT];
 #pragma unroll
@@ -247,22 +293,17 @@ __global__ void gather_coords_kernel(int64_t M, int dim, const int32_t *perm, co
     const int64_t q = q0 + (int64_t)u * blockDim.x;
     src[u] = q < M ? perm[q] : 0;
   }
-  T v0[PPT], v1[PPT], v2[PPT];
+  T v[PPT][DIM];
 #pragma unroll
-  for (int u = 0; u < PPT; u++) {
-    if (q0 + (int64_t)u * blockDim.x < M) {
-      v0[u] = rel0[src[u]];
-      v1[u] = dim >= 2 ? rel1[src[u]] : T(0);
-      v2[u] = dim == 3 ? rel2[src[u]] : T(0);
-    }
-  }
+  for (int u = 0; u < PPT; u++)
+    if (q0 + (int64_t)u * blockDim.x < M) R::load(rel + (int64_t)src[u] * R::PACK, v[u]);
+  T *const g[3] = {g0, g1, g2};
 #pragma unroll
   for (int u = 0; u < PPT; u++) {
     const int64_t q = q0 + (int64_t)u * blockDim.x;
     if (q < M) {
-      g0[q] = v0[u];
-      if (dim >= 2) g1[q] = v1[u];
-      if (dim == 3) g2[q] = v2[u];
+#pragma unroll
+      for (int d = 0; d < DIM; d++) g[d][q] = v[u][d];
     }
   }
 }
@@ -356,6 +397,35 @@ cudaError_t grow(Tptr **ptr, int64_t *cap, int64_t need, size_t elem) {
   return e;
 }
 
+template <typename T, int PPT>
+cudaError_t launch_cell_count(int dim, unsigned blocks, int threads, cudaStream_t s, const PointsIn &a,
+                              nufft_plan_s *p) {
+  T *rel = static_cast<T *>(p->gtmp);
+  if (dim == 1)
+    cell_count_kernel<T, 1, PPT><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag, rel);
+  else if (dim == 2)
+    cell_count_kernel<T, 2, PPT><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag, rel);
+  else
+    cell_count_kernel<T, 3, PPT><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag, rel);
+  return cudaGetLastError();
+}
+
+template <typename T, int PPT>
+cudaError_t launch_gather_coords(int dim, unsigned blocks, int threads, cudaStream_t s, int64_t M,
+                                 nufft_plan_s *p) {
+  const T *rel = static_cast<const T *>(p->gtmp);
+  T *g0 = static_cast<T *>(p->gcoord[0]);
+  T *g1 = static_cast<T *>(dim >= 2 ? p->gcoord[1] : p->gcoord[0]);
+  T *g2 = static_cast<T *>(dim == 3 ? p->gcoord[2] : p->gcoord[0]);
+  if (dim == 1)
+    gather_coords_kernel<T, 1, PPT><<<blocks, threads, 0, s>>>(M, p->perm, rel, g0, g1, g2);
+  else if (dim == 2)
+    gather_coords_kernel<T, 2, PPT><<<blocks, threads, 0, s>>>(M, p->perm, rel, g0, g1, g2);
+  else
+    gather_coords_kernel<T, 3, PPT><<<blocks, threads, 0, s>>>(M, p->perm, rel, g0, g1, g2);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
@@ -414,7 +484,8 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
   }
   if (!p->flag && cudaMalloc((void **)&p->flag, sizeof(int)) != cudaSuccess) return NUFFT_ERR_ALLOC;
   // caller-order bin-relative coordinates (dim arrays of M reals)
-  if (grow(&p->gtmp, &p->cap_gtmp, (int64_t)p->dim * (M > 0 ? M : 1), rs) != cudaSuccess)
+  const int pack = p->dim == 3 ? 4 : p->dim;  // CoordRec<T, dim>::PACK
+  if (grow(&p->gtmp, &p->cap_gtmp, (int64_t)pack * (M > 0 ? M : 1), rs) != cudaSuccess)
     return NUFFT_ERR_ALLOC;
 
   // --- 1. cells, bins and counts ------------------------------------------
@@ -436,19 +507,12 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
       cudaMemsetAsync(p->flag, 0, sizeof(int), s) != cudaSuccess)
     return NUFFT_ERR_CUDA;
   const int threads = 256;
-  void *rel[3];
-  for (int d = 0; d < 3; d++)
-    rel[d] = static_cast<char *>(p->gtmp) + (size_t)(d < p->dim ? d : 0) * (size_t)M * rs;
   if (M > 0) {
     constexpr int kPPT = 4;
     const unsigned blocks_cc = (unsigned)((M + threads * kPPT - 1) / (threads * kPPT));
-    if (p->dtype == 0)
-      cell_count_kernel<float, kPPT><<<blocks_cc, threads, 0, s>>>(
-          a, p->cell_counts, p->bin_of, p->rank_of, p->flag, (float *)rel[0], (float *)rel[1], (float *)rel[2]);
-    else
-      cell_count_kernel<double, kPPT><<<blocks_cc, threads, 0, s>>>(
-          a, p->cell_counts, p->bin_of, p->rank_of, p->flag, (double *)rel[0], (double *)rel[1], (double *)rel[2]);
-    if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
+    const cudaError_t e = p->dtype == 0 ? launch_cell_count<float, kPPT>(p->dim, blocks_cc, threads, s, a, p)
+                                        : launch_cell_count<double, kPPT>(p->dim, blocks_cc, threads, s, a, p);
+    if (e != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
   // --- 2. cell starts (bin starts are every cpb-th entry) -----------------
@@ -464,15 +528,9 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     constexpr int kPPT = 4;
     const unsigned blocks_ppt = (unsigned)((M + threads * kPPT - 1) / (threads * kPPT));
     cell_scatter_kernel<kPPT><<<blocks_ppt, threads, 0, s>>>(M, p->cell_starts, p->bin_of, p->rank_of, p->perm);
-    void *g1 = p->dim >= 2 ? p->gcoord[1] : p->gcoord[0], *g2 = p->dim == 3 ? p->gcoord[2] : p->gcoord[0];
-    if (p->dtype == 0)
-      gather_coords_kernel<float, kPPT><<<blocks_ppt, threads, 0, s>>>(
-          M, p->dim, p->perm, (const float *)rel[0], (const float *)rel[1], (const float *)rel[2],
-          (float *)p->gcoord[0], (float *)g1, (float *)g2);
-    else
-      gather_coords_kernel<double, kPPT><<<blocks_ppt, threads, 0, s>>>(
-          M, p->dim, p->perm, (const double *)rel[0], (const double *)rel[1], (const double *)rel[2],
-          (double *)p->gcoord[0], (double *)g1, (double *)g2);
+    if ((p->dtype == 0 ? launch_gather_coords<float, kPPT>(p->dim, blocks_ppt, threads, s, M, p)
+                       : launch_gather_coords<double, kPPT>(p->dim, blocks_ppt, threads, s, M, p)) != cudaSuccess)
+      return NUFFT_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
   }
 
