@@ -165,6 +165,34 @@ def load_traffic(kernel: str, workload: str):
     return e.get("dram_bytes_per_launch")
 
 
+_libcuda = None
+
+
+def reset_l2_priorities():
+    """Return the L2 lines that kernels marked evict-last to normal priority
+    (cuCtxResetPersistingL2Cache on the current context, which the CUDA
+    runtime made current for this thread), so that the flush that follows
+    evicts them too.  Returns the driver's status (0 = success)."""
+    global _libcuda
+    if _libcuda is None:
+        import ctypes
+        _libcuda = ctypes.CDLL("libcuda.so.1")
+    return _libcuda.cuCtxResetPersistingL2Cache()
+
+
+def flush_l2(flush, stream):
+    """Evict the previous step's data from L2 (untimed): demote evict-last
+    lines, then write a buffer larger than L2."""
+    import torch
+    torch.cuda.current_stream().synchronize()
+    stream.synchronize()
+    rc = reset_l2_priorities()
+    if rc != 0:
+        raise RuntimeError(f"cuCtxResetPersistingL2Cache failed: {rc}")
+    with torch.cuda.stream(stream):
+        flush.zero_()
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -375,8 +403,7 @@ def measure(wl, args, dev, stream, opts, steps: int, warmup: int, B: int = 1,
             clk.__enter__()
         try:
             for i in range(steps):
-                with torch.cuda.stream(stream):
-                    flush.zero_()                       # evict the inputs from L2 (untimed)
+                flush_l2(flush, stream)                 # evict the inputs from L2 (untimed)
                 ev0[i].record(stream)
                 step()
                 ev1[i].record(stream)
@@ -644,8 +671,7 @@ def run_sweep(args):
                 info = plan.info()
                 ms = []
                 for i in range(2 + steps):
-                    with torch.cuda.stream(stream):
-                        flush.zero_()
+                    flush_l2(flush, stream)
                     if t == 1:
                         plan.execute(c_in, f_out)
                     else:
