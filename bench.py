@@ -59,6 +59,8 @@ def parse():
                     help="time the spreading / interpolation kernel over a grid of plan options "
                          "(bins, M_sub, columns per lane, threads) for --workload, or for every "
                          "workload with --workload all; one JSON line per option set")
+    ap.add_argument("--sweep-type", type=int, choices=[1, 2], default=None,
+                    help="sweep only the type 1 (spreading) or type 2 (interpolation) plans")
     ap.add_argument("--cpu-sample", type=int, default=0,
                     help="points per transform in the CPU baseline sample (0: auto)")
     ap.add_argument("--sigma", type=float, default=2.0,
@@ -308,7 +310,7 @@ def run_reference(args, wl):
 
 # ------------------------------------------------------------------ GPU arm
 
-def kernel_names(wl: W.Workload, method1: int, method2: int, tile3d: int = 1) -> dict:
+def kernel_names(wl: W.Workload, method1: int, method2: int, tile3d: int = 1, igroup: int = 0) -> dict:
     """Names of the spreading and interpolation kernels the plans launch."""
     import nonuniform_fft_gb300 as nf
     df = "_df" if wl.dtype == "f64" else ""
@@ -317,7 +319,8 @@ def kernel_names(wl: W.Workload, method1: int, method2: int, tile3d: int = 1) ->
     spread = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
               nf.METHOD_GM: "spread_gmu_kernel", nf.METHOD_REGTILE: regtile}[method1]
     sm_interp = {1: "interp_sm1d_kernel", 2: "interp_sm_kernel",
-                 3: "interp_sm3d_df_kernel" if wl.dtype == "f64" else "interp_sm3d_bank_kernel"}
+                 3: "interp_sm3d_df_kernel" if wl.dtype == "f64" else
+                 ("interp_group3d_kernel" if igroup >= 2 else "interp_sm3d_bank_kernel")}
     interp = {nf.METHOD_GM_SORT: "interp_gm_kernel", nf.METHOD_GM: "interp_gmu_kernel"}.get(
         method2, sm_interp[wl.dim])
     return {"spread": spread, "interp": interp}
@@ -433,7 +436,8 @@ def measure(wl, args, dev, stream, opts, steps: int, warmup: int, B: int = 1,
         launches = -(-B // vpp)                           # spread / interp launches per transform
         algo = algorithmic_bytes(wl, n, vpp)
         peak, peak_source = hbm_peak()
-        names = kernel_names(wl, info["method"], info2["method"] if has2 else 0, info.get("tile3d", 1))
+        names = kernel_names(wl, info["method"], info2["method"] if has2 else 0, info.get("tile3d", 1),
+                             info2.get("igroup", 0) if has2 else 0)
         rooflines = {}
         for key in (("spread", "interp") if has2 else ("spread",)):
             ms = stage[key] / (steps * launches)
@@ -628,6 +632,9 @@ def sweep_space(wl: W.Workload, t: int) -> list:
                        grid(bin1=[16, 26, 32, 48], msub=[1024, 2048, 4096], threads=[128, 256, 512])]
     if wl.dim == 3 and t == 1:
         return [{}] + grid(bin2=[4, 8, 16, 32], msub=[2048, 4096, 8192])
+    if wl.dim == 3 and t == 2 and wl.dtype == "f32":   # one point per thread, or grouped by window
+        return ([{}] + grid(igroup=[1], msub=[2048, 4096, 8192], threads=[256, 512, 1024])
+                + grid(igroup=[2, 3, 4], msub=[2048, 4096, 8192], threads=[128, 256]))
     if wl.dim == 3 and t == 2:
         return [{}] + grid(msub=[2048, 4096, 8192], threads=[256, 512, 1024])
     if wl.dim == 1 and t == 1:
@@ -661,6 +668,8 @@ def run_sweep(args):
         stream.synchronize()
         steps = 3 if wl.dim == 3 and wl.dtype == "f64" else 6
         for t in wl.types:
+            if args.sweep_type and t != args.sweep_type:
+                continue
             for opts in sweep_space(wl, t):
                 try:
                     plan = nf.Plan(t, wl.N, wl.iflag[t], wl.eps, cname, stream=stream.cuda_stream, **opts)

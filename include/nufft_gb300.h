@@ -90,7 +90,9 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_I_FFT 13             /* 1: fused pruned FFT in use (option "fft"), 0: cuFFT */
 #define NUFFT_I_SMS 14             /* multiprocessors of the plan's device (sizes the default M_sub) */
 #define NUFFT_I_TILE3D 15          /* 3D REGTILE spreader in use: 1 planes per warp, 2 slab bins (0: not 3D) */
-#define NUFFT_I_COUNT 16
+#define NUFFT_I_IGROUP 16          /* 3D single-precision SM interpolator: 1 one point per thread,
+                                      K >= 2 points of one window origin per thread (0: other) */
+#define NUFFT_I_COUNT 17
 
 /* Spreading / interpolation methods (option "method"). */
 #define NUFFT_METHOD_AUTO 0
@@ -153,8 +155,9 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *   "threads"  threads per block of the SM / GM-sort spreading and
  *              interpolation kernels (multiple of 32, 32..1024; lowered to
  *              what a kernel's register use allows).  Default 256; for the
- *              3D shared-memory interpolators 512 (complex64) and 1024
- *              (complex128).
+ *              3D shared-memory interpolators 512 (complex64, one point per
+ *              thread) and 1024 (complex128); the grouped complex64
+ *              interpolator ("igroup") runs at most 256.
  *   "batch"    vectors per pass of nufft_execute_batch, 1..1024 (0: as many
  *              fine grids as fit in 1 GiB, at most 64).  Takes effect at the
  *              next execute.
@@ -167,6 +170,15 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *              cell thick in z (32 - 2 ceil(w/2) x 32 x 1 cells; complex64 and
  *              w <= 8 only, else BAD_OPT at setpts).  0 (default): 2 where it
  *              applies, else 1.
+ *   "igroup"   3D complex64 SM interpolation: 1, one thread per point; K = 2,
+ *              3 or 4, the points of one window origin (the w^3 nodes they
+ *              read) in groups of at most K per thread, each tile row loaded
+ *              once per group.  setpts reorders the points of each
+ *              subproblem by window origin and records the groups (w <= 8
+ *              and the build's shared memory -- one counter per origin, 20
+ *              bytes per point of M_sub -- within the device's limit, else
+ *              BAD_OPT at setpts).  0 (default): 2 where it applies, else 1.
+ *              Other plans ignore it.
  *   "fft"      0 (default): 2D complex64 plans whose fine grid sizes are
  *              powers of two from 256 to 4096 take the fine-grid FFT as two
  *              passes of the library's own kernels, pruned to the modes of

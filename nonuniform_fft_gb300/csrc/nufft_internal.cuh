@@ -23,7 +23,8 @@ struct Subproblem {
   int32_t bin;
   int32_t start;  // first sorted slot
   int32_t count;  // number of points
-  int32_t pad_;
+  int32_t groups;  // grouped 3D single-precision interpolation: window-origin groups
+                   // recorded for this subproblem (0 otherwise)
 };
 
 }  // namespace nufft
@@ -53,6 +54,8 @@ struct nufft_plan_s {
   int opt_batch = 0;           // vectors per pass of a batched execute (0: default)
   int opt_fft = 0;             // 0: fused pruned FFT where supported, 1: cuFFT
   int opt_tile3d = 0;          // 3D register-tile spreader: 0 auto, 1 planes per warp, 2 slab bins
+  int opt_igroup = 0;          // 3D single-precision SM interpolation: 0 auto, 1 one point per thread,
+                               // 2..4 points sharing a window per thread
 
   // --- resolved at setpts ------------------------------------------------
   int method = NUFFT_METHOD_SM;
@@ -62,6 +65,8 @@ struct nufft_plan_s {
   int threads = 256;
   int regtile_cols = 4;        // tile columns per lane of the register-tile spreader
   int tile3d = 1;              // 3D register-tile spreader in use: 1 planes per warp, 2 slab bins
+  int igroup = 0;              // 3D f32 SM interpolator in use: 1 one point per thread, K >= 2 groups
+                               // of at most K points (0: another interpolator)
   int64_t nbins = 0;
   int64_t nsub = 0;
   int64_t M = 0;
@@ -91,6 +96,8 @@ struct nufft_plan_s {
   void *gtmp = nullptr;            // setpts scratch: dim x M bin-relative coordinates, caller order
   int64_t cap_gtmp = 0;
   nufft::Subproblem *subprob = nullptr;
+  uint32_t *grec = nullptr;        // grouped interpolation: one record per group, at the
+  int64_t cap_grec = 0;            // sorted slots of its subproblem (interp_group3d_f32.cu)
   int64_t cap_sub = 0;
   int *flag = nullptr;             // device error flag (setpts)
   void *stage_c = nullptr;         // staging for host c
@@ -150,6 +157,14 @@ constexpr int kSlab3DMaxWidth = 8;
 bool slab3d_supported(int w, int dtype);
 void slab3d_bins(int w, int *m1, int *m2, int *m3);
 cudaError_t launch_spread_slab3d(const nufft_plan_s *p, const void *c);
+// 3D single-precision interpolation with tile reads shared by points of one
+// window origin (interp_group3d_f32.cu): supported for w <= kGroup3DMaxWidth
+// when its shared memory fits (p->m and p->msub resolved), group size p->igroup.
+constexpr int kGroup3DMaxWidth = 8;
+constexpr int kGroup3DDefault = 2;  // option sweep: 2.42 ms (K = 2), 2.46 (3, 4), 3.20 (1)
+bool group3d_supported(const nufft_plan_s *p, int smem_max);
+cudaError_t build_groups3d(const nufft_plan_s *p);
+cudaError_t launch_interp_group3d(const nufft_plan_s *p, void *c);
 
 // spreadinterp_1d.cu: 1D register-tile spreading and shared-memory interpolation.
 cudaError_t launch_spread_1d(const nufft_plan_s *p, const void *c);

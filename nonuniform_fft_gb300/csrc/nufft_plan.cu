@@ -196,6 +196,7 @@ void release(nufft_plan_s *p) {
   cudaFree(p->rank_of);
   cudaFree(p->gtmp);
   cudaFree(p->subprob);
+  cudaFree(p->grec);
   cudaFree(p->flag);
   cudaFree(p->stage_c);
   cudaFree(p->stage_f);
@@ -409,6 +410,9 @@ int nufft_set_opt(nufft_plan_t p, const char *key, double value) {
   } else if (!std::strcmp(key, "tile3d")) {
     if (v < 0 || v > 2) return NUFFT_ERR_BAD_OPT;
     p->opt_tile3d = (int)v;
+  } else if (!std::strcmp(key, "igroup")) {
+    if (v < 0 || v > 4) return NUFFT_ERR_BAD_OPT;
+    p->opt_igroup = (int)v;
   } else if (!std::strcmp(key, "threads")) {
     if (v != 0 && (v < 32 || v > 1024 || v % 32)) return NUFFT_ERR_BAD_OPT;
     p->opt_threads = (int)v;
@@ -506,11 +510,21 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   if (p->method == NUFFT_METHOD_GM && nufft::grid_cells(p) >= (int64_t(1) << 31)) return NUFFT_ERR_TOO_LARGE;
   // the cell-level sort indexes (bin, cell) pairs with int32
   if (p->nbins * (int64_t)m[0] * m[1] * m[2] >= (int64_t(1) << 31) - 1) return NUFFT_ERR_TOO_LARGE;
+  // 3D single-precision SM interpolation: points grouped by window origin
+  // where the kernel's shared memory fits (the default), else one point per
+  // thread
+  p->igroup = 0;
+  if (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM && p->dtype == 0) {
+    const bool ok = nufft::group3d_supported(p, smem_max);
+    if (p->opt_igroup >= 2 && !ok) return NUFFT_ERR_BAD_OPT;
+    p->igroup = p->opt_igroup == 1 ? 1 : (p->opt_igroup >= 2 ? p->opt_igroup : (ok ? nufft::kGroup3DDefault : 1));
+  }
   // the 3D interpolators hold one large tile per block (two blocks per SM in
   // single precision, one in double): more threads per block keep more warps
-  // per SM busy (512 and 1024 from the option sweeps)
+  // per SM busy (512 and 1024 from the option sweeps); the grouped kernel
+  // holds K points' weights per thread and runs 256
   const int def_threads = (p->dim == 3 && p->type == 2 && p->method == NUFFT_METHOD_SM)
-                              ? (p->dtype == 0 ? 512 : 1024)
+                              ? (p->dtype == 0 ? (p->igroup >= 2 ? 256 : 512) : 1024)
                               : 256;
   p->threads = p->opt_threads > 0 ? p->opt_threads : def_threads;
   p->fused_fft = p->opt_fft == 0 && p->fft_tw != nullptr;
@@ -631,6 +645,7 @@ int nufft_execute_batch(nufft_plan_t p, int64_t nvec, void *c, void *f) {
     auto interp = [&]() -> cudaError_t {
       if (p->M == 0 || (p->method != NUFFT_METHOD_GM && p->nsub == 0)) return cudaSuccess;
       if (p->dim == 1) return nufft::launch_interp_1d(p, dc);
+      if (p->igroup >= 2) return nufft::launch_interp_group3d(p, dc);
       if (p->dim == 2)
         return p->dtype == 0 ? nufft::launch_interp_t<2, float>(p, dc) : nufft::launch_interp_t<2, double>(p, dc);
       return p->dtype == 0 ? nufft::launch_interp_t<3, float>(p, dc) : nufft::launch_interp_t<3, double>(p, dc);
@@ -723,7 +738,7 @@ int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
   if (!p || !info || n < 0) return NUFFT_ERR_BAD_ARG;
   const int64_t v[NUFFT_I_COUNT] = {p->w,    p->n[0], p->n[1], p->n[2], p->M,      p->nbins,  p->nsub,
                                     p->m[0], p->m[1], p->m[2], p->msub, p->method, batch_pass(p),
-                                    p->fused_fft ? 1 : 0, p->num_sms, p->dim == 3 ? p->tile3d : 0};
+                                    p->fused_fft ? 1 : 0, p->num_sms, p->dim == 3 ? p->tile3d : 0, p->igroup};
   for (int i = 0; i < n && i < NUFFT_I_COUNT; i++) info[i] = v[i];
   return NUFFT_OK;
 }

@@ -367,7 +367,7 @@ __global__ void sub_fill_kernel(const int32_t *counts, const int32_t *starts,
   e.start = starts[b] + k * msub;
   const int32_t left = counts[b] - k * msub;
   e.count = left < msub ? left : msub;
-  e.pad_ = 0;
+  e.groups = 0;
   table[s] = e;
 }
 
@@ -552,6 +552,12 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     sub_fill_kernel<<<(unsigned)((p->nsub + threads - 1) / threads), threads, 0, s>>>(
         p->bin_counts, p->bin_starts, p->sub_starts, p->nbins, p->nsub, p->msub, p->subprob);
     if (cudaGetLastError() != cudaSuccess) return NUFFT_ERR_CUDA;
+  }
+
+  // --- 5. window-origin groups of the grouped 3D interpolator -------------
+  if (p->igroup >= 2) {
+    if (grow(&p->grec, &p->cap_grec, M > 0 ? M : 1, sizeof(uint32_t)) != cudaSuccess) return NUFFT_ERR_ALLOC;
+    if (build_groups3d(p) != cudaSuccess) return NUFFT_ERR_CUDA;
   }
   return NUFFT_OK;
 }

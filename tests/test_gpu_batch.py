@@ -64,6 +64,7 @@ CASES = [
     (2, (100, 70), "f64", 1e-6, {"method": nf.METHOD_GM}),
     (2, (100, 70), "f32", 1e-5, {"regtile_cols": 2}),
     (3, (20, 24, 36), "f32", 1e-6, {}),
+    (3, (20, 24, 36), "f32", 1e-6, {"igroup": 1}),
     (3, (20, 24, 36), "f64", 1e-12, {}),
     (3, (20, 24, 36), "f32", 1e-4, {"method": nf.METHOD_SM}),
     (3, (20, 24, 36), "f64", 1e-9, {"method": nf.METHOD_GM}),

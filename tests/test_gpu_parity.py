@@ -503,3 +503,94 @@ def test_interp3d_large_msub_is_capped():
     c = gpu_transform(2, pts, fk, N, 1e-5, 1, "f32", {"msub": 100000}, plan_out=info)
     assert info["msub"] == 8192
     assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, 1e-5, 1)) <= TOL_O2["f32"]
+
+
+def _stacked_pts(M, rng, nodes=5):
+    """3D points piled on a few spots (each spot's points share one window
+    origin, so one origin holds far more than a group's K points), plus a
+    uniform half."""
+    spots = rng.uniform(-np.pi, np.pi, (3, nodes))
+    pick = rng.integers(0, nodes, M // 2)
+    pts = []
+    for d in range(3):
+        a = rng.uniform(-np.pi, np.pi, M)
+        a[: M // 2] = spots[d][pick] + rng.uniform(-1e-4, 1e-4, M // 2)
+        pts.append(a.astype(np.float32))
+    return pts
+
+
+@pytest.mark.parametrize("K", [2, 3, 4])
+@pytest.mark.parametrize("eps", [1e-2, 1e-5, 1e-6, 1e-7])
+@pytest.mark.parametrize("N,dist,opts", [((20, 24, 36), "uniform", {}),
+                                         ((33, 18, 16), "cluster", {}),
+                                         ((30, 22, 26), "stacked", {"msub": 37}),
+                                         ((20, 24, 36), "uniform", {"msub": 8192, "bin1": 7, "bin2": 9,
+                                                                   "bin3": 5})])
+def test_group3d_interp(K, eps, N, dist, opts):
+    """3D single-precision interpolation with the points of one window origin
+    in groups of at most K per thread (option igroup; widths 3, 6, 7 and 8
+    here): against the oracle's three-step NUFFT, and bit for bit against
+    one thread per point (igroup = 1), which sums the same products in the
+    same order."""
+    rng = np.random.default_rng(47)
+    M = 40000
+    pts = _stacked_pts(M, rng) if dist == "stacked" else _pts(3, M, dist, rng, "f32")
+    fk = _cplx(int(np.prod(N)), rng, "f32")
+    info = {}
+    c = gpu_transform(2, pts, fk, N, eps, 1, "f32", dict(opts, igroup=K), plan_out=info)
+    assert info["igroup"] == K
+    assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, eps, 1)) <= TOL_O2["f32"]
+    info1 = {}
+    c1 = gpu_transform(2, pts, fk, N, eps, 1, "f32", dict(opts, igroup=1), plan_out=info1)
+    assert info1["igroup"] == 1
+    np.testing.assert_array_equal(c, c1)
+
+
+@pytest.mark.parametrize("M", [1, 3, 33])
+def test_group3d_interp_few_points(M):
+    """Subproblems of one to a few dozen points (most groups of one point,
+    most warps partly empty)."""
+    rng = np.random.default_rng(48)
+    N = (16, 12, 10)
+    pts = _pts(3, M, "uniform", rng, "f32")
+    fk = _cplx(int(np.prod(N)), rng, "f32")
+    c = gpu_transform(2, pts, fk, N, 1e-6, -1, "f32", {"igroup": 4})
+    assert oracle.rel_l2(c, oracle.nufft_type2(pts, fk, N, 1e-6, -1)) <= TOL_O2["f32"]
+
+
+def test_group3d_interp_defaults_and_rejection():
+    """Grouped interpolation is the default for 3D single-precision type 2
+    plans with w <= 8 (groups of 2); other plans report igroup 0; asking for
+    groups where the kernel cannot run (w = 10) fails at setpts."""
+    xf = torch.zeros(10, dtype=torch.float32, device=DEV)
+    with nf.Plan(2, (8, 8, 8), 1, 1e-6, "complex64") as plan:
+        plan.setpts(xf, xf, xf)
+        assert plan.info()["igroup"] == 2
+    with nf.Plan(2, (8, 8, 8), 1, 1e-9, "complex64") as plan:     # w = 10
+        plan.setpts(xf, xf, xf)
+        assert plan.info()["igroup"] == 1
+    with nf.Plan(1, (8, 8, 8), 1, 1e-6, "complex64") as plan:
+        plan.setpts(xf, xf, xf)
+        assert plan.info()["igroup"] == 0
+    with nf.Plan(2, (8, 8, 8), 1, 1e-9, "complex64", igroup=3) as plan:
+        with pytest.raises(nf.NufftError) as e:
+            plan.setpts(xf, xf, xf)
+        assert e.value.code == nf.ERR_BAD_OPT
+
+
+def test_group3d_interp_plan_reuse():
+    """One grouped 3D plan, setpts with more, fewer and again more points
+    (the group records are rebuilt, and their storage grown, each time)."""
+    rng = np.random.default_rng(49)
+    N = (18, 20, 16)
+    with nf.Plan(2, N, 1, 1e-6, "complex64") as plan:
+        for M in (20000, 700, 45000):
+            pts = _pts(3, M, "uniform", rng, "f32")
+            plan.setpts(*[torch.from_numpy(p).to(DEV) for p in pts])
+            assert plan.info()["igroup"] == 2
+            for _ in range(2):
+                fk = _cplx(int(np.prod(N)), rng, "f32")
+                c = torch.zeros(M, dtype=torch.complex64, device=DEV)
+                plan.execute(c, torch.from_numpy(fk).to(DEV))
+                ref = oracle.nufft_type2(pts, fk, N, 1e-6, 1)
+                assert oracle.rel_l2(c.cpu().numpy(), ref) <= TOL_O2["f32"]
