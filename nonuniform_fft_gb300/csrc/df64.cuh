@@ -93,6 +93,25 @@ DF_HD void df_fma(DF &acc, DF a, DF b) {
   acc = df_quick(s, e);
 }
 
+// acc += a * b without renormalising: acc.hi takes the float sum, and the
+// exact TwoSum error of that addition plus the product's own error terms go
+// to acc.lo in float arithmetic, so acc.hi + acc.lo carries the running sum
+// while |acc.lo| grows by at most one unit in the last place of acc.hi per
+// step.  After n steps the float rounding of acc.lo is below n^2 2^-48 of
+// the largest partial sum; callers renormalise (df_sum) after a short run,
+// at most 16 terms.
+DF_HD void df_fma_lazy(DF &acc, DF a, DF b) {
+  const float p = DF_MUL(a.hi, b.hi);
+  float pe = DF_FMA(a.hi, b.hi, -p);
+  pe = DF_FMA(a.hi, b.lo, pe);
+  pe = DF_FMA(a.lo, b.hi, pe);
+  const float s = DF_ADD(acc.hi, p);
+  const float v = DF_SUB(s, acc.hi);
+  const float e = DF_ADD(DF_SUB(acc.hi, DF_SUB(s, v)), DF_SUB(p, v));
+  acc.hi = s;
+  acc.lo = DF_ADD(acc.lo, DF_ADD(e, pe));
+}
+
 // a + b.
 DF_HD DF df_sum(DF a, DF b) {
   const float s = DF_ADD(a.hi, b.hi);

@@ -517,7 +517,7 @@ struct DFC2 {  // complex two-float, 16 bytes
 };
 
 template <int W>
-__global__ void interp_sm3d_df_kernel(SIParams<double> a) {
+__global__ void __launch_bounds__(640, 1) interp_sm3d_df_kernel(SIParams<double> a) {
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_out += blockIdx.y * a.cstride;
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -573,17 +573,18 @@ __global__ void interp_sm3d_df_kernel(SIParams<double> a) {
 #pragma unroll
       for (int i2 = 0; i2 < W; i2++) {
         const DFC2 *row = tile + ((s3 + i3) * p2 + s2 + i2) * p1 + s1;
-        // two independent chains per component (even and odd i1)
+        // two independent chains per component (even and odd i1), each at
+        // most 8 terms, renormalised when the two are added
         DF sr0{0.f, 0.f}, si0{0.f, 0.f}, sr1{0.f, 0.f}, si1{0.f, 0.f};
 #pragma unroll
         for (int i1 = 0; i1 < W; i1 += 2) {
           const DFC2 b = row[i1];
-          df_fma(sr0, b.re, kx[i1]);
-          df_fma(si0, b.im, kx[i1]);
+          df_fma_lazy(sr0, b.re, kx[i1]);
+          df_fma_lazy(si0, b.im, kx[i1]);
           if (i1 + 1 < W) {
             const DFC2 c = row[i1 + 1];
-            df_fma(sr1, c.re, kx[i1 + 1]);
-            df_fma(si1, c.im, kx[i1 + 1]);
+            df_fma_lazy(sr1, c.re, kx[i1 + 1]);
+            df_fma_lazy(si1, c.im, kx[i1 + 1]);
           }
         }
         df_fma(r3, df_sum(sr0, sr1), ky[i2]);

@@ -53,3 +53,58 @@ def test_df64_es_kernel_accuracy(driver):
     for (z, beta), g in zip(cases, got):
         ref = _exact(z, beta)
         assert abs(g - ref) <= 8e-15, (z, beta, g, ref)
+
+
+@pytest.fixture(scope="module")
+def dot_driver(tmp_path_factory):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path_factory.mktemp("df64dot") / "drv")
+    subprocess.run([nvcc, "-O2", "-std=c++17", "-Xcompiler", "-ffp-contract=off",
+                    os.path.join(HERE, "host", "df64_dot_driver.cu"), "-o", exe],
+                   check=True, capture_output=True)
+    return exe
+
+
+def test_df64_lazy_dot_products(dot_driver):
+    """Row sums of the double-precision interpolator: up to 16 products of
+    two-floats, accumulated without renormalisation in two chains and
+    renormalised once, against the exact sum of the same two-float products
+    (Fraction arithmetic).  The bound is relative to the sum of |terms|: two
+    two-float roundings per product (2^-47 each) plus the deferred float
+    rounding of the low parts.  The renormalising form df_fma is held to the
+    same bound."""
+    from fractions import Fraction
+
+    def split(x):
+        hi = float(np.float32(x))
+        lo = float(np.float32(x - hi))
+        return hi, lo
+
+    rng = np.random.default_rng(7)
+    lines, cases = [], []
+    for n in list(range(1, 17)) * 12:
+        kind = rng.integers(0, 3)
+        a = rng.standard_normal(n) * (10.0 ** rng.uniform(-3, 3, n) if kind == 2 else 1.0)
+        b = np.abs(rng.uniform(0, 1, n)) if kind != 1 else rng.standard_normal(n)
+        if kind == 1 and n > 1:              # heavy cancellation
+            a[-1] = -sum(a[:-1] * b[:-1]) / b[-1]
+        lines.append(f"{n} " + " ".join(f"{float(x)!r} {float(y)!r}" for x, y in zip(a, b)))
+        cases.append((a, b))
+    out = subprocess.run([dot_driver], input="\n".join(lines) + "\n", capture_output=True, text=True,
+                         check=True).stdout.strip().splitlines()
+    assert len(out) == len(cases)
+    for (a, b), line in zip(cases, out):
+        lh, ll, sh, sl = (float(v) for v in line.split())
+        exact = Fraction(0)
+        mag = Fraction(0)
+        for x, y in zip(a, b):
+            xh, xl = split(x)
+            yh, yl = split(y)
+            t = (Fraction(xh) + Fraction(xl)) * (Fraction(yh) + Fraction(yl))
+            exact += t
+            mag += abs(t)
+        bound = float(mag) * 2.0 ** -44
+        assert abs(float(Fraction(lh) + Fraction(ll) - exact)) <= bound, (len(a), lh, ll, float(exact))
+        assert abs(float(Fraction(sh) + Fraction(sl) - exact)) <= bound, (len(a), sh, sl, float(exact))
