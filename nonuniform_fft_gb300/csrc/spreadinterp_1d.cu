@@ -89,16 +89,24 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_kernel(Params1D<T>
     grid_atomic_add(a.grid + wrap_tile(sp.bin * a.m1 + x_rel, a.n1), ar, ai);
 }
 
+// A complex two-float, 16-byte aligned so that it moves as one 16-byte
+// shared-memory access.
+struct __align__(16) DFC16 {
+  DF re, im;
+};
+
 // Double precision: each point's w+1 extended kernel values are evaluated
 // once, in two-float arithmetic (df64.cuh), when its batch is staged, and
-// stored as products c_j phi; a lane-visit is then one 16-byte load and two
-// adds (evaluating the kernel per lane-visit in double cost w+1 double
-// exp/sqrt pairs per point on this part's small FP64 rate).
+// stored as two-float products c_j phi; a lane-visit is then one 16-byte
+// load and two two-float adds.  Only the coordinate split and the final
+// column sum touch the FP64 pipe, which this part runs at 1/64 of the FP32
+// rate (native double products and sums per slot and per lane-visit kept it
+// busy 84 % of the time and took 1.48 ms on the 1D workload).
 template <int W>
 __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_df_kernel(Params1D<double> a) {
   constexpr int PAD = (W + 1) / 2, HW = W / 2, WX = W + 1, WCS = WX | 1;
   constexpr int S = W <= 8 ? 64 : 32;
-  __shared__ double2 s_cw[kWarps1D][S][WCS];
+  __shared__ DFC16 s_cw[kWarps1D][S][WCS];
   __shared__ int s_xb[kWarps1D][S];
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
@@ -119,17 +127,20 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_df_kernel(Params1D
     lhi = cs[xw_hi] < hi ? cs[xw_hi] : hi;
   }
   const DF beta = df_from(a.beta_e);
-  double ar = 0.0, ai = 0.0;
+  DF ar{0.f, 0.f}, ai{0.f, 0.f};
   for (int bs = lo; bs < hi; bs += S) {
     const int nb = (bs + S < hi ? bs + S : hi) - bs;
     for (int q = lane; q < nb; q += 32) {
       const double2 cv = ld_hint(a.c_in + ld_hint(a.perm + bs + q, pol_stream), pol_keep);
       DF ext[WX];
       s_xb[warp][q] = es_extended_df<W, WX>(ld_hint(a.g1 + bs + q, pol_stream), beta, ext);
+      const DF cr = df_from(cv.x), ci = df_from(cv.y);
 #pragma unroll
       for (int e = 0; e < WX; e++) {
-        const double w = df_to(ext[e]);
-        s_cw[warp][q][e] = make_double2(cv.x * w, cv.y * w);
+        DFC16 v;
+        v.re = df_mul(cr, ext[e]);
+        v.im = df_mul(ci, ext[e]);
+        s_cw[warp][q][e] = v;
       }
     }
     __syncwarp();
@@ -138,15 +149,17 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_df_kernel(Params1D
       const int q = j - bs;
       int e = x_rel - s_xb[warp][q];
       e = e < 0 ? 0 : (e > W ? W : e);
-      const double2 v = s_cw[warp][q][e];
-      ar += v.x;
-      ai += v.y;
+      const DFC16 v = s_cw[warp][q][e];
+      ar = df_sum(ar, v.re);
+      ai = df_sum(ai, v.im);
     }
     __syncwarp();
   }
-  if (ar != 0.0 || ai != 0.0) grid_atomic_add(a.grid + wrap_tile(sp.bin * a.m1 + x_rel, a.n1), ar, ai);
+  const double vr = df_to(ar), vi = df_to(ai);
+  if (vr != 0.0 || vi != 0.0) grid_atomic_add(a.grid + wrap_tile(sp.bin * a.m1 + x_rel, a.n1), vr, vi);
 }
 
+// Single precision (double: interp_sm1d_df_kernel below).
 template <typename T, int W>
 __global__ void interp_sm1d_kernel(Params1D<T> a) {
   using CT = typename Cplx<T>::type;
@@ -164,15 +177,7 @@ __global__ void interp_sm1d_kernel(Params1D<T> a) {
   const int end = sp.start + sp.count;
   for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
     T k1[W];
-    int s1;
-    if constexpr (std::is_same<T, double>::value) {
-      DF kd[W];
-      s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), df_from(a.beta_e), kd) + PAD;
-#pragma unroll
-      for (int t = 0; t < W; t++) k1[t] = df_to(kd[t]);
-    } else {
-      s1 = es_weights<T, W>(ld_hint(a.g1 + j, pol_stream), a.beta_e, k1) + PAD;
-    }
+    const int s1 = es_weights<T, W>(ld_hint(a.g1 + j, pol_stream), a.beta_e, k1) + PAD;
     T ar = T(0), ai = T(0);
 #pragma unroll
     for (int i1 = 0; i1 < W; i1++) {
@@ -183,6 +188,49 @@ __global__ void interp_sm1d_kernel(Params1D<T> a) {
     CT out;
     out.x = ar;
     out.y = ai;
+    st_hint(a.c_out + ld_hint(a.perm + j, pol_stream), out, pol_keep);
+  }
+}
+
+// Double precision: the padded bin is staged as two-floats and the w
+// multiply-adds run in two-float arithmetic on the FP32 pipes (df64.cuh);
+// the kernel values come from the same two-float evaluation as the
+// spreader's.  At most 16 terms: accumulated without renormalisation
+// (df_fma_lazy), the sum hi + lo converted to double exactly.
+template <int W>
+__global__ void interp_sm1d_df_kernel(Params1D<double> a) {
+  a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
+  a.c_out += blockIdx.y * a.cstride;
+  constexpr int PAD = (W + 1) / 2;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  DFC16 *tile = reinterpret_cast<DFC16 *>(smem_raw);
+  const Subproblem sp = a.sub[blockIdx.x];
+  const int p1 = a.m1 + 2 * PAD;
+  const int o1 = sp.bin * a.m1 - PAD;
+  for (int s = threadIdx.x; s < p1; s += blockDim.x) {
+    const double2 v = a.grid[wrap_tile(o1 + s, a.n1)];
+    DFC16 d;
+    d.re = df_from(v.x);
+    d.im = df_from(v.y);
+    tile[s] = d;
+  }
+  __syncthreads();
+  const uint64_t pol_stream = l2_evict_first(), pol_keep = l2_evict_last();
+  const DF beta = df_from(a.beta_e);
+  const int end = sp.start + sp.count;
+  for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
+    DF k1[W];
+    const int s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), beta, k1) + PAD;
+    DF ar{0.f, 0.f}, ai{0.f, 0.f};
+#pragma unroll
+    for (int i1 = 0; i1 < W; i1++) {
+      const DFC16 b = tile[s1 + i1];
+      df_fma_lazy(ar, b.re, k1[i1]);
+      df_fma_lazy(ai, b.im, k1[i1]);
+    }
+    double2 out;
+    out.x = df_to(ar);
+    out.y = df_to(ai);
     st_hint(a.c_out + ld_hint(a.perm + j, pol_stream), out, pol_keep);
   }
 }
@@ -211,13 +259,10 @@ cudaError_t spread1d_w(const nufft_plan_s *p, const void *c) {
   Params1D<T> a = params1d<T>(p);
   a.c_in = static_cast<const typename Cplx<T>::type *>(c);
   const dim3 grid((unsigned)((p->nsub + kWarps1D - 1) / kWarps1D), p->nvec);
-  if constexpr (std::is_same<T, double>::value) {
+  if constexpr (std::is_same<T, double>::value)
     spread_reg1d_df_kernel<W><<<grid, 32 * kWarps1D, 0, p->stream>>>(a);
-    return cudaGetLastError();
-  }
-  spread_reg1d_kernel<T, W><<<grid,
-                              32 * kWarps1D, 0,
-                              p->stream>>>(a);
+  else
+    spread_reg1d_kernel<T, W><<<grid, 32 * kWarps1D, 0, p->stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -225,11 +270,20 @@ template <typename T, int W>
 cudaError_t interp1d_w(const nufft_plan_s *p, void *c) {
   Params1D<T> a = params1d<T>(p);
   a.c_out = static_cast<typename Cplx<T>::type *>(c);
-  const size_t smem = (size_t)(p->m[0] + 2 * ((W + 1) / 2)) * 2 * sizeof(T);
-  cudaError_t e = allow_smem(interp_sm1d_kernel<T, W>, smem);
-  if (e != cudaSuccess) return e;
-  interp_sm1d_kernel<T, W><<<dim3((unsigned)p->nsub, p->nvec), block_threads(interp_sm1d_kernel<T, W>, p->threads),
-                             smem, p->stream>>>(a);
+  if constexpr (std::is_same<T, double>::value) {
+    const size_t smem = (size_t)(p->m[0] + 2 * ((W + 1) / 2)) * sizeof(DFC16);
+    cudaError_t e = allow_smem(interp_sm1d_df_kernel<W>, smem);
+    if (e != cudaSuccess) return e;
+    interp_sm1d_df_kernel<W><<<dim3((unsigned)p->nsub, p->nvec), block_threads(interp_sm1d_df_kernel<W>, p->threads),
+                               smem, p->stream>>>(a);
+    return cudaGetLastError();
+  } else {
+    const size_t smem = (size_t)(p->m[0] + 2 * ((W + 1) / 2)) * 2 * sizeof(T);
+    cudaError_t e = allow_smem(interp_sm1d_kernel<T, W>, smem);
+    if (e != cudaSuccess) return e;
+    interp_sm1d_kernel<T, W><<<dim3((unsigned)p->nsub, p->nvec), block_threads(interp_sm1d_kernel<T, W>, p->threads),
+                               smem, p->stream>>>(a);
+  }
   return cudaGetLastError();
 }
 
