@@ -168,6 +168,43 @@ DF_HD DF df_exp(DF a) {
   return DF{ldexpf(p.hi, k), ldexpf(p.lo, k)};
 }
 
+// A table of 2^(j/64), j = 0..63, shortens the series: a = (64 k + j) ln2/64
+// + r with |r| <= ln2/128 (Cody-Waite with ln2/64 split in three floats, the
+// first with 11 significant bits so that n times it is exact for |n| < 2^13),
+// e^r by its Taylor series to degree 6 (truncation below 3e-20), then e^a =
+// 2^k 2^(j/64) e^r.  The table entries come from df_exp of the arguments
+// j ln2/64, formed from the same split (df_exp2_64).
+constexpr double kLn2Over64 = 0.693147180559945309417232121458176568 / 64;
+constexpr float kL64a = 0.010833740234375f;  // 1420 / 2^17
+constexpr float kL64b = (float)(kLn2Over64 - (double)kL64a);
+constexpr float kL64c = (float)(kLn2Over64 - (double)kL64a - (double)kL64b);
+
+DF_HD DF df_exp2_64(int j) {
+  const float jf = (float)j;
+  DF arg{DF_MUL(jf, kL64a), 0.f};  // exact: 6 + 11 bits
+  arg = df_sum(arg, df_mul(DF{jf, 0.f}, DF{kL64b, 0.f}));
+  arg = df_sum(arg, df_mul(DF{jf, 0.f}, DF{kL64c, 0.f}));
+  return df_exp(arg);
+}
+
+DF_HD DF df_exp_tab(DF a, const DF *tab) {
+  const float nf = rintf(DF_MUL(a.hi, 92.33248261689366f));  // 64 / ln2
+  DF r = df_sum(a, DF{DF_MUL(-nf, kL64a), 0.f});             // exact product
+  r = df_sum(r, df_neg(df_mul(DF{nf, 0.f}, DF{kL64b, 0.f})));
+  r = df_sum(r, df_neg(df_mul(DF{nf, 0.f}, DF{kL64c, 0.f})));
+  constexpr double F[7] = {1.0, 1.0, 1.0 / 2, 1.0 / 6, 1.0 / 24, 1.0 / 120, 1.0 / 720};
+  DF p{(float)F[6], (float)(F[6] - (double)(float)F[6])};
+#pragma unroll
+  for (int n = 5; n >= 0; n--) {
+    const DF c{(float)F[n], (float)(F[n] - (double)(float)F[n])};
+    p = df_sum(df_mul(p, r), c);
+  }
+  const int n = (int)nf;
+  p = df_mul(p, tab[n & 63]);  // n = 64 (n >> 6) + (n & 63)
+  const int k = n >> 6;
+  return DF{ldexpf(p.hi, k), ldexpf(p.lo, k)};
+}
+
 // The ES kernel phi(z) = exp(beta (sqrt(1 - z^2) - 1)) (eq. (5)) for |z| <= 1,
 // with the exponent written -beta z^2 / (1 + sqrt(1 - z^2)) so that nothing
 // cancels near z = 0, and 1 - z^2 as (1 - z)(1 + z) so that nothing cancels
@@ -179,6 +216,16 @@ DF_HD DF df_es_kernel(DF z, DF beta) {
   const DF z2 = df_mul(z, z);
   const DF ex = df_neg(df_mul(beta, df_div(z2, df_sum(one, s))));
   return df_exp(ex);
+}
+
+// The same with the table exponential (tab: the 64 values of df_exp2_64).
+DF_HD DF df_es_kernel(DF z, DF beta, const DF *tab) {
+  const DF one{1.f, 0.f};
+  const DF om = df_mul(df_sum(one, df_neg(z)), df_sum(one, z));
+  const DF s = df_sqrt(om);
+  const DF z2 = df_mul(z, z);
+  const DF ex = df_neg(df_mul(beta, df_div(z2, df_sum(one, s))));
+  return df_exp_tab(ex, tab);
 }
 
 }  // namespace nufft

@@ -321,6 +321,8 @@ __global__ void __launch_bounds__(Plane3DDF<W, Z, K>::THREADS, 1)
   auto &s_xb = stg.xb;
   __shared__ int r_lo[G::M3], r_hi[G::M3], r_pos[G::M3 + 1];
   __shared__ int r_cs[G::M3][G::M1 + 1];
+  __shared__ DF s_exp2[64];
+  fill_exp2_64(s_exp2);  // read after the first barrier below
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Subproblem sp = a.sub[blockIdx.x];
@@ -390,20 +392,23 @@ __global__ void __launch_bounds__(Plane3DDF<W, Z, K>::THREADS, 1)
         const double gx = ld_hint(a.g1 + j, pol_stream), gy = ld_hint(a.g2 + j, pol_stream),
                      gz = ld_hint(a.g3 + j, pol_stream);
         // one dimension at a time, so only one array of kernel values is live
-        // next to the accumulators
-        double ek[G::WX];
-        es_extended<double, W, G::WX>(gy, a.beta_e, ek);
+        // next to the accumulators; two-float kernel values and products
+        // (native double here kept the FP64 pipe a quarter busy)
+        const DF beta = df_from(a.beta_e);
+        DF ek[G::WX];
+        es_extended_df<W, G::WX>(gy, beta, ek, s_exp2);
 #pragma unroll
-        for (int t = 0; t < G::WX; t++) s_wy[q][t] = df_from(ek[t]);
-        es_extended<double, W, G::WX>(gz, a.beta_e, ek);
+        for (int t = 0; t < G::WX; t++) s_wy[q][t] = ek[t];
+        es_extended_df<W, G::WX>(gz, beta, ek, s_exp2);
 #pragma unroll
-        for (int t = 0; t < G::WX; t++) s_wz[q][t] = df_from(ek[t]);
-        s_xb[q] = es_extended<double, W, G::WX>(gx, a.beta_e, ek);
+        for (int t = 0; t < G::WX; t++) s_wz[q][t] = ek[t];
+        s_xb[q] = es_extended_df<W, G::WX>(gx, beta, ek, s_exp2);
+        const DF cr = df_from(cv.x), ci = df_from(cv.y);
 #pragma unroll
         for (int t = 0; t < G::WX; t++) {
           DFC pr;
-          pr.re = df_from(cv.x * ek[t]);
-          pr.im = df_from(cv.y * ek[t]);
+          pr.re = df_mul(cr, ek[t]);
+          pr.im = df_mul(ci, ek[t]);
           s_cwx[q][t] = pr;
         }
       }

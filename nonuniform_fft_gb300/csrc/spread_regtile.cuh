@@ -89,11 +89,11 @@ struct __align__(16) RegStage {
 
 // es_extended in two-float arithmetic (double-precision plans).
 template <int W, int WX>
-__device__ __forceinline__ int es_extended_df(double g, DF beta, DF (&ext)[WX]) {
+__device__ __forceinline__ int es_extended_df(double g, DF beta, DF (&ext)[WX], const DF *exp2_64) {
   constexpr int HW = W / 2;
   const double cellf = floor(g);
   DF k[W];
-  const int l0 = es_weights_df<W>(g, beta, k);
+  const int l0 = es_weights_df<W>(g, beta, k, exp2_64);
   const int shift = l0 - ((int)cellf - HW);  // 0 or 1
 #pragma unroll
   for (int s = 0; s < WX; s++) {

@@ -72,15 +72,23 @@ __device__ __forceinline__ int es_weights(T g, T beta_e, T (&k)[W]) {
 }
 
 // The same w kernel values in two-float arithmetic (double-precision plans):
-// l0 = ceil(g - w/2) in double, then phi((l0 - g + t) 2/w) by df_es_kernel.
+// l0 = ceil(g - w/2) in double, then phi((l0 - g + t) 2/w) by df_es_kernel
+// with the table exponential (exp2_64: the 64 values of df_exp2_64, which
+// the calling kernel keeps in shared memory).
 template <int W>
-__device__ __forceinline__ int es_weights_df(double g, DF beta, DF (&k)[W]) {
+__device__ __forceinline__ int es_weights_df(double g, DF beta, DF (&k)[W], const DF *exp2_64) {
   const double l0 = ceil(g - 0.5 * W);
   const DF d = df_from(l0 - g);
   const DF scale = df_from(2.0 / W);
 #pragma unroll
-  for (int t = 0; t < W; t++) k[t] = df_es_kernel(df_mul(df_sum(d, DF{(float)t, 0.f}), scale), beta);
+  for (int t = 0; t < W; t++)
+    k[t] = df_es_kernel(df_mul(df_sum(d, DF{(float)t, 0.f}), scale), beta, exp2_64);
   return (int)l0;
+}
+
+// Fill a block's shared table of 2^(j/64) (before its first barrier).
+__device__ __forceinline__ void fill_exp2_64(DF *tab) {
+  for (int j = threadIdx.x; j < 64; j += blockDim.x) tab[j] = df_exp2_64(j);
 }
 
 // L2 cache policies.  Points are streamed once per transform (evict first);
@@ -522,6 +530,8 @@ __global__ void __launch_bounds__(640, 1) interp_sm3d_df_kernel(SIParams<double>
   a.c_out += blockIdx.y * a.cstride;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   DFC2 *tile = reinterpret_cast<DFC2 *>(smem_raw);
+  __shared__ DF s_exp2[64];
+  fill_exp2_64(s_exp2);
   constexpr int PAD = (W + 1) / 2;
   const Subproblem sp = a.sub[blockIdx.x];
   int b1, b2, b3;
@@ -562,9 +572,9 @@ __global__ void __launch_bounds__(640, 1) interp_sm3d_df_kernel(SIParams<double>
   for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
     DF kx[W], ky[W], kz[W];
     const DF beta = df_from(a.beta);
-    const int s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), beta, kx) + PAD;
-    const int s2 = es_weights_df<W>(ld_hint(a.g2 + j, pol_stream), beta, ky) + PAD;
-    const int s3 = es_weights_df<W>(ld_hint(a.g3 + j, pol_stream), beta, kz) + PAD;
+    const int s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), beta, kx, s_exp2) + PAD;
+    const int s2 = es_weights_df<W>(ld_hint(a.g2 + j, pol_stream), beta, ky, s_exp2) + PAD;
+    const int s3 = es_weights_df<W>(ld_hint(a.g3 + j, pol_stream), beta, kz, s_exp2) + PAD;
     const int dst = ld_hint(a.perm + j, pol_stream);
     DF ar{0.f, 0.f}, ai{0.f, 0.f};
 #pragma unroll 1

@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_df_kernel(Params1D
   constexpr int S = W <= 8 ? 64 : 32;
   __shared__ DFC16 s_cw[kWarps1D][S][WCS];
   __shared__ int s_xb[kWarps1D][S];
+  __shared__ DF s_exp2[64];
+  fill_exp2_64(s_exp2);
+  __syncthreads();
   a.grid += blockIdx.y * a.gstride;  // vector blockIdx.y of a batched launch
   a.c_in += blockIdx.y * a.cstride;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(32 * kWarps1D) spread_reg1d_df_kernel(Params1D
     for (int q = lane; q < nb; q += 32) {
       const double2 cv = ld_hint(a.c_in + ld_hint(a.perm + bs + q, pol_stream), pol_keep);
       DF ext[WX];
-      s_xb[warp][q] = es_extended_df<W, WX>(ld_hint(a.g1 + bs + q, pol_stream), beta, ext);
+      s_xb[warp][q] = es_extended_df<W, WX>(ld_hint(a.g1 + bs + q, pol_stream), beta, ext, s_exp2);
       const DF cr = df_from(cv.x), ci = df_from(cv.y);
 #pragma unroll
       for (int e = 0; e < WX; e++) {
@@ -204,6 +207,8 @@ __global__ void interp_sm1d_df_kernel(Params1D<double> a) {
   constexpr int PAD = (W + 1) / 2;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   DFC16 *tile = reinterpret_cast<DFC16 *>(smem_raw);
+  __shared__ DF s_exp2[64];
+  fill_exp2_64(s_exp2);
   const Subproblem sp = a.sub[blockIdx.x];
   const int p1 = a.m1 + 2 * PAD;
   const int o1 = sp.bin * a.m1 - PAD;
@@ -220,7 +225,7 @@ __global__ void interp_sm1d_df_kernel(Params1D<double> a) {
   const int end = sp.start + sp.count;
   for (int j = sp.start + threadIdx.x; j < end; j += blockDim.x) {
     DF k1[W];
-    const int s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), beta, k1) + PAD;
+    const int s1 = es_weights_df<W>(ld_hint(a.g1 + j, pol_stream), beta, k1, s_exp2) + PAD;
     DF ar{0.f, 0.f}, ai{0.f, 0.f};
 #pragma unroll
     for (int i1 = 0; i1 < W; i1++) {

@@ -45,14 +45,17 @@ def test_df64_es_kernel_accuracy(driver):
             cases += [(float(z), beta) for z in rng.uniform(-1, 1, 20)]
     inp = "".join(f"{z!r} {b!r}\n" for z, b in cases)
     out = subprocess.run([driver], input=inp, capture_output=True, text=True, check=True).stdout
-    got = [float(a) + float(b) for a, b in (line.split() for line in out.strip().splitlines())]
+    rows = [[float(v) for v in line.split()] for line in out.strip().splitlines()]
+    assert len(rows) == len(cases)
     # absolute error, i.e. relative to the kernel's peak phi(0) = 1: that is
     # the error a weighted sum sees.  A double-precision evaluation of the
     # same formula is off by up to about beta * 1e-16 * phi (~4e-15); the
-    # two-float one carries 48 bits and stays below 8e-15.
-    for (z, beta), g in zip(cases, got):
+    # two-float one carries 48 bits and stays below 8e-15, with the series
+    # exponential and with the table one (2^(j/64) and a degree-6 series).
+    for (z, beta), (sh, sl, th, tl) in zip(cases, rows):
         ref = _exact(z, beta)
-        assert abs(g - ref) <= 8e-15, (z, beta, g, ref)
+        assert abs((sh + sl) - ref) <= 8e-15, (z, beta, sh + sl, ref)
+        assert abs((th + tl) - ref) <= 8e-15, ("table", z, beta, th + tl, ref)
 
 
 @pytest.fixture(scope="module")
