@@ -65,6 +65,7 @@ struct nufft_plan_s {
   int threads = 256;
   int regtile_cols = 4;        // tile columns per lane of the register-tile spreader
   int tile3d = 1;              // 3D register-tile spreader in use: 1 planes per warp, 2 slab bins
+  bool bin_origin = false;     // points binned by window origin (the slab spreader), not by cell
   int igroup = 0;              // 3D f32 SM interpolator in use: 1 one point per thread, K >= 2 groups
                                // of at most K points (0: another interpolator)
   int64_t nbins = 0;

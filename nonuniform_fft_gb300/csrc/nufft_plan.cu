@@ -444,6 +444,7 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
   for (int d = 0; d < 3; d++)
     if (d < p->dim && p->opt_bin[d] > 0) m[d] = p->opt_bin[d];
   p->regtile_cols = p->opt_regtile_cols > 0 ? p->opt_regtile_cols : 1;
+  p->bin_origin = false;
   if (p->dim == 1) {
     // one padded-bin column per lane for spreading; long bins for the
     // interpolator's staged tile, short enough in single precision that the
@@ -462,6 +463,7 @@ int nufft_setpts(nufft_plan_t p, int64_t M, const void *x, const void *y, const 
       const bool slab_ok = nufft::slab3d_supported(p->w, p->dtype);
       if (p->opt_tile3d == 2 && !slab_ok) return NUFFT_ERR_BAD_OPT;
       p->tile3d = p->opt_tile3d == 1 ? 1 : (slab_ok ? 2 : 1);
+      p->bin_origin = p->tile3d == 2;  // the slab spreader bins points by window origin
       if (p->tile3d == 2)
         nufft::slab3d_bins(p->w, &m[0], &m[1], &m[2]);
       else

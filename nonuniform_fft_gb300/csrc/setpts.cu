@@ -29,6 +29,8 @@ struct PointsIn {
   double inv_two_pi;
   float turn3[3];  // inv_two_pi split exactly into three floats (fold_fast)
   int fast;        // 1: turn3 is exact, so fold_fast may be used
+  int origin;      // 1: bin by window origin (origin_node), 0: by cell
+  float oc;        // origin_node offset: 1/2 for odd w, 0 for even w
   int n[3];
   int m[3];
   int nb[3];
@@ -72,8 +74,8 @@ __device__ __forceinline__ void two_sum(float a, float b, float *hi, float *lo) 
 // not finite, |x| > 1024, n >= 2^24, or g is that close to a cell boundary
 // (about 1e-8 of the coordinates at n = 2048).  Otherwise sets the cell and
 // gh + gl (no part of the integer result depends on gl beyond the check).
-__device__ __forceinline__ bool fold_fast(float x, const float (&c)[3], int n, int *cell, float *gh,
-                                          float *gl) {
+__device__ __forceinline__ bool fold_fast_hl(float x, const float (&c)[3], int n, float *gh, float *gl,
+                                             float *delta) {
   if (!(fabsf(x) <= 1024.0f) || n >= (1 << 24)) return false;
   const float p0 = x * c[0], e0 = fmaf(x, c[0], -p0);
   const float p1 = x * c[1], e1 = fmaf(x, c[1], -p1);
@@ -96,17 +98,43 @@ __device__ __forceinline__ bool fold_fast(float x, const float (&c)[3], int n, i
   }
   const float nf = (float)n;
   const float h = s * nf;
-  const float l = fmaf(s, nf, -h) + sl * nf;
+  *gl = fmaf(s, nf, -h) + sl * nf;
+  *gh = h;
+  *delta = nf * (fabsf(p0) + 1.0f) * 5.6843419e-14f;  // n (|x c| + 1) 2^-44
+  return true;
+}
+
+// The cell floor(g) of g = gh + gl (fold_fast_hl), when g is farther than
+// delta from every integer.
+__device__ __forceinline__ bool cell_from_hl(float h, float l, float delta, int n, int *cell) {
   const float r = rintf(h);
   const float d = (h - r) + l;  // h - r is exact
-  const float delta = nf * (fabsf(p0) + 1.0f) * 5.6843419e-14f;  // n (|x c| + 1) 2^-44
   if (fabsf(d) <= delta) return false;
   const int k = (int)r - (d < 0.0f ? 1 : 0);
   if (k < 0 || k >= n) return false;
   *cell = k;
-  *gh = h;
-  *gl = l;
   return true;
+}
+
+// The node ceil(g - oc), in [0, n], of g = gh + gl (fold_fast_hl), when g -
+// oc is farther than delta from every integer (oc = 1/2 or 0; h - 1/2 is
+// exact below 2^22).
+__device__ __forceinline__ bool node_from_hl(float h, float l, float delta, float oc, int n, int *node) {
+  if (oc != 0.0f && n > (1 << 22)) return false;
+  const float h2 = h - oc;
+  const float r = rintf(h2);
+  const float d = (h2 - r) + l;
+  if (fabsf(d) <= delta) return false;
+  const int k = (int)r + (d > 0.0f ? 1 : 0);
+  if (k < 0 || k > n) return false;
+  *node = k;
+  return true;
+}
+
+__device__ __forceinline__ bool fold_fast(float x, const float (&c)[3], int n, int *cell, float *gh,
+                                          float *gl) {
+  float delta;
+  return fold_fast_hl(x, c, n, gh, gl, &delta) && cell_from_hl(*gh, *gl, delta, n, cell);
 }
 
 template <typename T>
@@ -181,8 +209,17 @@ struct CoordRec {
   }
 };
 
+__device__ __forceinline__ float above(float v) { return nextafterf(v, INFINITY); }
+__device__ __forceinline__ double above(double v) { return ::nextafter(v, (double)INFINITY); }
+
 // Key and bin-relative coordinates of point j (see cell_count_kernel).
-template <typename T, int DIM>
+// ORIGIN false: the point is binned by its cell floor(g).  ORIGIN true: by
+// the node q = ceil(g - oc) mod n (oc = 1/2 for odd w, 0 for even w), which
+// is ceil(g - w/2) + floor(w/2), the first node of its support shifted by
+// floor(w/2); its bin-relative coordinate v is then kept in (q_rel - 1 + oc,
+// q_rel + oc], where ceil(v - w/2) + floor(w/2) = q_rel, and is taken one
+// period down when q wrapped from n to 0.
+template <typename T, int DIM, bool ORIGIN>
 __device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T (&out)[DIM], bool *bad) {
   int bin = 0, stride = 1, local = 0, lstride = 1;
 #pragma unroll
@@ -191,16 +228,33 @@ __device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T (&ou
     T v = T(0);
     bool done = false;
     if constexpr (std::is_same<T, float>::value) {
-      float gh, gl;
-      if (a.fast && fold_fast(static_cast<const float *>(a.x[d])[j], a.turn3, a.n[d], &cell, &gh, &gl)) {
-        v = (gh - (float)((cell / a.m[d]) * a.m[d])) + gl;  // the difference is exact
-        done = true;
+      float gh, gl, delta;
+      if (a.fast && fold_fast_hl(static_cast<const float *>(a.x[d])[j], a.turn3, a.n[d], &gh, &gl, &delta)) {
+        if constexpr (!ORIGIN) {
+          if (cell_from_hl(gh, gl, delta, a.n[d], &cell)) {
+            v = (gh - (float)((cell / a.m[d]) * a.m[d])) + gl;  // the difference is exact
+            done = true;
+          }
+        } else if (node_from_hl(gh, gl, delta, a.oc, a.n[d], &cell)) {
+          const float hw = cell == a.n[d] ? gh - (float)a.n[d] : gh;  // exact
+          if (cell == a.n[d]) cell = 0;
+          v = (hw - (float)((cell / a.m[d]) * a.m[d])) + gl;
+          done = true;
+        }
       }
     }
     if (!done) {
-      const double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], bad);
-      cell = (int)floor(g);
-      if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
+      double g = grid_coord(load_coord<T>(a.x[d], j), a.inv_two_pi, a.n[d], bad);
+      if constexpr (!ORIGIN) {
+        cell = (int)floor(g);
+        if (cell >= a.n[d]) cell = a.n[d] - 1;  // unreachable; keeps the index in range
+      } else {
+        cell = (int)ceil(g - (double)a.oc);
+        if (cell >= a.n[d]) {
+          cell = 0;
+          g -= (double)a.n[d];
+        }
+      }
       v = (T)(g - (double)((cell / a.m[d]) * a.m[d]));  // exact in double, then rounded to T
     }
     const int b = cell / a.m[d];
@@ -209,8 +263,14 @@ __device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T (&ou
     stride *= a.nb[d];
     local += cell_rel * lstride;
     lstride *= a.m[d];
-    if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
-    if (v < (T)cell_rel) v = (T)cell_rel;
+    if constexpr (!ORIGIN) {
+      if (floor(v) > (T)cell_rel) v = below(T(cell_rel + 1));
+      if (v < (T)cell_rel) v = (T)cell_rel;
+    } else {
+      const T hi_v = (T)cell_rel + (T)a.oc;
+      if (v > hi_v) v = hi_v;
+      if (v <= hi_v - T(1)) v = above(hi_v - T(1));
+    }
     out[d] = v;
   }
   return bin * lstride + local;
@@ -226,7 +286,7 @@ __device__ __forceinline__ int32_t cell_key(const PointsIn &a, int64_t j, T (&ou
 // (CoordRec), and later gathered into sorted order.  Each thread takes PPT
 // points blockDim.x apart and issues their counter increments back to back,
 // so that several returning atomics are in flight per thread.
-template <typename T, int DIM, int PPT>
+template <typename T, int DIM, int PPT, bool ORIGIN>
 __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, int32_t *rank_of,
                                   int *flag, T *rel) {
   using R = CoordRec<T, DIM>;
@@ -239,7 +299,7 @@ __global__ void cell_count_kernel(PointsIn a, int32_t *counts, int32_t *key_of, 
     key[u] = 0;
     if (j < a.M) {
       T v[DIM];
-      key[u] = cell_key<T, DIM>(a, j, v, &bad);
+      key[u] = cell_key<T, DIM, ORIGIN>(a, j, v, &bad);
       R::store(rel + j * R::PACK, v);
     }
   }
@@ -402,11 +462,17 @@ cudaError_t launch_cell_count(int dim, unsigned blocks, int threads, cudaStream_
                               nufft_plan_s *p) {
   T *rel = static_cast<T *>(p->gtmp);
   if (dim == 1)
-    cell_count_kernel<T, 1, PPT><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag, rel);
+    cell_count_kernel<T, 1, PPT, false><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of,
+                                                                   p->flag, rel);
   else if (dim == 2)
-    cell_count_kernel<T, 2, PPT><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag, rel);
+    cell_count_kernel<T, 2, PPT, false><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of,
+                                                                   p->flag, rel);
+  else if (!a.origin)
+    cell_count_kernel<T, 3, PPT, false><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of,
+                                                                   p->flag, rel);
   else
-    cell_count_kernel<T, 3, PPT><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of, p->flag, rel);
+    cell_count_kernel<T, 3, PPT, true><<<blocks, threads, 0, s>>>(a, p->cell_counts, p->bin_of, p->rank_of,
+                                                                  p->flag, rel);
   return cudaGetLastError();
 }
 
@@ -489,7 +555,7 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
     return NUFFT_ERR_ALLOC;
 
   // --- 1. cells, bins and counts ------------------------------------------
-  PointsIn a;
+  PointsIn a{};
   a.x[0] = x;
   a.x[1] = y;
   a.x[2] = p->dim == 3 ? z : x;
@@ -498,6 +564,8 @@ int run_setpts(nufft_plan_s *p, const void *x, const void *y, const void *z) {
   a.is_double = p->dtype;
   a.inv_two_pi = 1.0 / (2.0 * 3.14159265358979323846);
   split_turn(a);
+  a.origin = p->bin_origin ? 1 : 0;
+  a.oc = p->w % 2 ? 0.5f : 0.0f;
   for (int d = 0; d < 3; d++) {
     a.n[d] = (int)p->n[d];
     a.m[d] = p->m[d];
@@ -585,7 +653,7 @@ int run_setpts_gm(nufft_plan_s *p, const void *x, const void *y, const void *z) 
     p->cap_pts = M;
   }
   if (!p->flag && cudaMalloc((void **)&p->flag, sizeof(int)) != cudaSuccess) return NUFFT_ERR_ALLOC;
-  PointsIn a;
+  PointsIn a{};
   a.x[0] = x;
   a.x[1] = y;
   a.x[2] = p->dim == 3 ? z : x;
@@ -691,7 +759,7 @@ extern "C" int nufft_binsort_noalloc(int dim, int dtype, int64_t M, const void *
   if ((dim != 2 && dim != 3) || (dtype != 0 && dtype != 1) || M < 0 || !n_fine || !bins ||
       !counts || (M > 0 && (!x || !y || (dim == 3 && !z) || !perm)))
     return NUFFT_ERR_BAD_ARG;
-  PointsIn a;
+  PointsIn a{};
   for (int d = 0; d < 3; d++) {
     const int64_t n = d < dim ? n_fine[d] : 1, m = d < dim ? bins[d] : 1;
     if (n < 1 || m < 1 || n > (int64_t(1) << 30)) return NUFFT_ERR_BAD_ARG;

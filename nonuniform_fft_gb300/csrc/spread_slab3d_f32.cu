@@ -5,12 +5,13 @@ namespace nufft {
 
 bool slab3d_supported(int w, int dtype) { return dtype == 0 && w >= 2 && w <= kSlab3DMaxWidth; }
 
-// Bins one cell thick in z, 32 - 2 ceil(w/2) cells wide (lane L owns padded
-// column L), 32 rows (rows only slide the register windows; measured on the
-// 3D single-precision workload at w = 7 with one subproblem per bin: 4, 8,
-// 12, 16, 24, 32, 48 rows gave 5.61, 5.13, 4.99, 4.91, 4.87, 4.84, 4.96 ms).
+// Bins one window origin thick in z, 33 - w origins wide (lane L owns padded
+// column L: w - 1 columns of padding), 32 rows (rows only slide the register
+// windows; measured on the 3D single-precision workload at w = 7 with one
+// subproblem per bin and cell binning: 4, 8, 12, 16, 24, 32, 48 rows gave
+// 5.61, 5.13, 4.99, 4.91, 4.87, 4.84, 4.96 ms).
 void slab3d_bins(int w, int *m1, int *m2, int *m3) {
-  *m1 = 32 - 2 * ((w + 1) / 2);
+  *m1 = 33 - w;
   *m2 = 32;
   *m3 = 1;
 }

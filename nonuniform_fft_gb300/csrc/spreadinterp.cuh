@@ -71,6 +71,15 @@ __device__ __forceinline__ int es_weights(T g, T beta_e, T (&k)[W]) {
   return (int)l0;
 }
 
+// The same for a given first node l0 (the caller's window origin).
+template <typename T, int W>
+__device__ __forceinline__ void es_weights_at(T g, int l0, T beta_e, T (&k)[W]) {
+  const T d = T(l0) - g;
+  const T scale = T(2) / T(W);
+#pragma unroll
+  for (int t = 0; t < W; t++) k[t] = es_fast((d + T(t)) * scale, beta_e);
+}
+
 // The same w kernel values in two-float arithmetic (double-precision plans):
 // l0 = ceil(g - w/2) in double, then phi((l0 - g + t) 2/w) by df_es_kernel
 // with the table exponential (exp2_64: the 64 values of df_exp2_64, which

@@ -108,6 +108,8 @@ def _load():
     lib.oracle_interp.restype = None
     lib.oracle_binsort.argtypes = [I, P, P, I64, P, P, P, P, P, P, P]
     lib.oracle_binsort.restype = I64
+    lib.oracle_binsort_origin.argtypes = [I, P, P, I, I64, P, P, P, P, P, P, P]
+    lib.oracle_binsort_origin.restype = I64
     lib.oracle_subproblems.argtypes = [I64, P, P, I64, P]
     lib.oracle_subproblems.restype = I64
     lib.oracle_gauss_legendre.argtypes = [I, P, P]
@@ -450,9 +452,14 @@ def grid_coord(x: float, n: int) -> float:
     return _load().oracle_grid_coord(float(x), int(n))
 
 
-def binsort(pts, n, m, msub: int):
+def binsort(pts, n, m, msub: int, origin_w: int = 0):
     """Bin of each point, bin counts, bin starts, the stable permutation t and
-    the subproblem table (bin, first sorted slot, count) rows."""
+    the subproblem table (bin, first sorted slot, count) rows.
+
+    origin_w = 0: a point's bin is the bin of its cell floor(g) ([cuFINUFFT]
+    Sec. III-A).  origin_w = w > 0: the bin of its window origin shifted by
+    floor(w/2), (ceil(g - w/2) + floor(w/2)) mod n, with ceil(g - w/2) the
+    first of the w nodes the point touches (Sec. II-B)."""
     dim, x, y, z = _coords(pts)
     nn = np.asarray(list(n), dtype=np.int64)
     mm = np.asarray(list(m), dtype=np.int64)
@@ -463,8 +470,12 @@ def binsort(pts, n, m, msub: int):
     starts = np.zeros(nbins, np.int32)
     perm = np.zeros(x.size, np.int32)
     lib = _load()
-    lib.oracle_binsort(dim, _ptr(nn), _ptr(mm), x.size, _ptr(x), _ptr(y), _ptr(z),
-                       _ptr(bin_of), _ptr(counts), _ptr(starts), _ptr(perm))
+    if origin_w:
+        lib.oracle_binsort_origin(dim, _ptr(nn), _ptr(mm), int(origin_w), x.size, _ptr(x), _ptr(y),
+                                  _ptr(z), _ptr(bin_of), _ptr(counts), _ptr(starts), _ptr(perm))
+    else:
+        lib.oracle_binsort(dim, _ptr(nn), _ptr(mm), x.size, _ptr(x), _ptr(y), _ptr(z),
+                           _ptr(bin_of), _ptr(counts), _ptr(starts), _ptr(perm))
     nsub = lib.oracle_subproblems(nbins, _ptr(counts), _ptr(starts), int(msub), None)
     table = np.zeros((nsub, 3), np.int32)
     lib.oracle_subproblems(nbins, _ptr(counts), _ptr(starts), int(msub), _ptr(table))

@@ -327,18 +327,36 @@ void oracle_interp(int dim, const int64_t *n, int w, double beta, int64_t M,
  * counting sort; the paper leaves the order inside a bin open).
  * Returns the number of bins.
  */
-int64_t oracle_binsort(int dim, const int64_t *n, const int64_t *m, int64_t M,
-                       const double *x, const double *y, const double *z,
-                       int32_t *bin_of, int32_t *counts, int32_t *starts,
-                       int32_t *perm) {
+/*
+ * The grid index a point is binned by: its cell floor(g) (w == 0, the
+ * paper's bin of a point), or, with w > 0, the node l0 + floor(w/2) (mod n)
+ * where l0 = ceil(g - w/2) is the first node of its support (support()
+ * above): the bin then holds the point's window origin shifted by
+ * floor(w/2), so the window lies inside the bin padded by floor(w/2) nodes
+ * on the left and w - 1 - floor(w/2) on the right.  l0 + floor(w/2) =
+ * ceil(g - oc) with oc = w/2 - floor(w/2) (1/2 or 0); it is evaluated in
+ * that form, where no rounding enters (g - 3, say, rounds for g below about
+ * 2e-16 and would move such a point's node by one).
+ */
+static int64_t bin_index(double x, int64_t n, int w) {
+    const double g = oracle_grid_coord(x, n);
+    if (w == 0) return (int64_t)floor(g);
+    const double oc = 0.5 * (double)w - (double)(w / 2);
+    return wrap((int64_t)ceil(g - oc), n);
+}
+
+static int64_t binsort_by(int dim, const int64_t *n, const int64_t *m, int w, int64_t M,
+                          const double *x, const double *y, const double *z,
+                          int32_t *bin_of, int32_t *counts, int32_t *starts,
+                          int32_t *perm) {
     int64_t nb[3] = {1, 1, 1};
     for (int i = 0; i < dim; i++) nb[i] = (n[i] + m[i] - 1) / m[i];
     int64_t nbins = nb[0] * nb[1] * nb[2];
     for (int64_t b = 0; b < nbins; b++) counts[b] = 0;
     for (int64_t j = 0; j < M; j++) {
-        int64_t c1 = (int64_t)floor(oracle_grid_coord(x[j], n[0]));
-        int64_t c2 = dim >= 2 ? (int64_t)floor(oracle_grid_coord(y[j], n[1])) : 0;
-        int64_t c3 = dim == 3 ? (int64_t)floor(oracle_grid_coord(z[j], n[2])) : 0;
+        int64_t c1 = bin_index(x[j], n[0], w);
+        int64_t c2 = dim >= 2 ? bin_index(y[j], n[1], w) : 0;
+        int64_t c3 = dim == 3 ? bin_index(z[j], n[2], w) : 0;
         int64_t b1 = c1 / m[0], b2 = dim >= 2 ? c2 / m[1] : 0, b3 = dim == 3 ? c3 / m[2] : 0;
         int64_t b = b1 + nb[0] * (b2 + nb[1] * b3);
         bin_of[j] = (int32_t)b;
@@ -354,6 +372,21 @@ int64_t oracle_binsort(int dim, const int64_t *n, const int64_t *m, int64_t M,
     for (int64_t j = 0; j < M; j++) perm[fill[bin_of[j]]++] = (int32_t)j;
     free(fill);
     return nbins;
+}
+
+int64_t oracle_binsort(int dim, const int64_t *n, const int64_t *m, int64_t M,
+                       const double *x, const double *y, const double *z,
+                       int32_t *bin_of, int32_t *counts, int32_t *starts,
+                       int32_t *perm) {
+    return binsort_by(dim, n, m, 0, M, x, y, z, bin_of, counts, starts, perm);
+}
+
+/* The same with points binned by window origin (bin_index with w > 0). */
+int64_t oracle_binsort_origin(int dim, const int64_t *n, const int64_t *m, int w, int64_t M,
+                              const double *x, const double *y, const double *z,
+                              int32_t *bin_of, int32_t *counts, int32_t *starts,
+                              int32_t *perm) {
+    return binsort_by(dim, n, m, w, M, x, y, z, bin_of, counts, starts, perm);
 }
 
 /*

@@ -43,8 +43,9 @@ def _two_sum(a, b):
     return s, lo
 
 
-def fold_fast(x, n):
-    """(ok, cell) of the float fold for float32 x and grid size n."""
+def _fold_hl(x, n):
+    """The float fold's g = h + l and its error bound delta (eligible where
+    |x| <= 1024)."""
     x = x.astype(F)
     c0, c1, c2 = (np.full_like(x, v) for v in _split3())
     p0 = (x * c0).astype(F)
@@ -63,12 +64,30 @@ def fold_fast(x, n):
     nf = F(n)
     h = (s * nf).astype(F)
     l = (_fma(s, np.full_like(s, nf), -h) + (sl * nf).astype(F)).astype(F)
+    delta = (nf * (np.abs(p0) + F(1)) * F(5.6843419e-14)).astype(F)
+    return np.abs(x) <= 1024, h, l, delta
+
+
+def fold_fast(x, n):
+    """(ok, cell) of the float fold for float32 x and grid size n."""
+    elig, h, l, delta = _fold_hl(x, n)
     r = np.rint(h).astype(F)
     d = ((h - r) + l).astype(F)
-    delta = (nf * (np.abs(p0) + F(1)) * F(5.6843419e-14)).astype(F)
     k = r.astype(np.int64) - (d < 0)
-    ok = (np.abs(x) <= 1024) & (np.abs(d) > delta) & (k >= 0) & (k < n)
+    ok = elig & (np.abs(d) > delta) & (k >= 0) & (k < n)
     return ok, k
+
+
+def node_fast(x, n, oc):
+    """(ok, node) of the float fold's window-origin node ceil(g - oc), oc =
+    1/2 (odd w) or 0 (even w), taken mod n."""
+    elig, h, l, delta = _fold_hl(x, n)
+    h2 = (h - F(oc)).astype(F)
+    r = np.rint(h2).astype(F)
+    d = ((h2 - r) + l).astype(F)
+    k = r.astype(np.int64) + (d > 0)
+    ok = elig & (np.abs(d) > delta) & (k >= 0) & (k <= n) & ((oc == 0) | (n <= 1 << 22))
+    return ok, np.where(k == n, 0, k)
 
 
 def cell_double(x, n):
@@ -78,6 +97,16 @@ def cell_double(x, n):
     g = t * float(n)
     g = np.where(g >= n, g - n, g)
     return np.floor(g).astype(np.int64)
+
+
+def node_double(x, n, w):
+    """The oracle's bin index by window origin, ceil(g - w/2) + floor(w/2) =
+    ceil(g - oc) (mod n), from the double fold."""
+    t = x.astype(np.float64) * C
+    t = t - np.floor(t)
+    g = t * float(n)
+    g = np.where(g >= n, g - n, g)
+    return np.mod(np.ceil(g - (0.5 * w - w // 2)).astype(np.int64), n)
 
 
 def test_double_fold_restatement_matches_oracle():
@@ -125,3 +154,40 @@ def test_float_fold_cells_equal_double_fold(n):
     # random coordinates almost never need the double fold
     okr, _ = fold_fast(xs[0], n)
     assert okr.mean() > 0.9999
+
+
+def _half_boundary_floats(n, per_side=3):
+    """The float32 values nearest the coordinates 2 pi (k + 1/2) / n (the
+    origin boundaries of odd w), and one period either side."""
+    k = np.arange(n + 1, dtype=np.float64) + 0.5
+    out = []
+    for shift in (0.0, -2 * np.pi, 2 * np.pi):
+        v = (2 * np.pi * k / n + shift).astype(F)
+        out.append(v)
+        lo, hi = v.copy(), v.copy()
+        for _ in range(per_side):
+            lo = np.nextafter(lo, F(-np.inf))
+            hi = np.nextafter(hi, F(np.inf))
+            out += [lo.copy(), hi.copy()]
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("w", [7, 6, 3, 8])
+@pytest.mark.parametrize("n", [128, 256, 2048, 1280])
+def test_float_fold_origins_equal_double_fold(n, w):
+    """setpts bins the slab spreader's points by window origin: the node
+    ceil(g - oc) (oc = 1/2 for odd w, 0 for even w) from the float fold,
+    where it answers, equals the double fold's ceil(g - w/2) + floor(w/2)
+    (mod n), on random coordinates and on the floats nearest the origin
+    boundaries (half-integer g for odd w, integer g for even w)."""
+    rng = np.random.default_rng(n + w)
+    oc = 0.5 if w % 2 else 0.0
+    x = np.concatenate([rng.uniform(-np.pi, np.pi, 1_000_000).astype(F),
+                        rng.uniform(-1024, 1024, 100_000).astype(F),
+                        _half_boundary_floats(n) if w % 2 else _boundary_floats(n),
+                        np.array([0.0, -0.0, np.pi, -np.pi, 2 * np.pi], dtype=F)])
+    ok, k = node_fast(x, n, oc)
+    ref = node_double(x, n, w)
+    bad = ok & (k != ref)
+    assert not bad.any(), f"n={n} w={w}: {bad.sum()} origins differ, e.g. x={x[bad][:5]}"
+    assert ok[:1_000_000].mean() > 0.9999

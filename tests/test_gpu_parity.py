@@ -110,7 +110,9 @@ def test_setpts_integer_results_match_oracle(dim, N, M, dist, dt, opts):
         got = plan.sort()
     n = [info["n1"], info["n2"], info["n3"]][:dim]
     m = [info["bin1"], info["bin2"], info["bin3"]][:dim]
-    ref = oracle.binsort(pts, n, m, info["msub"])
+    # the 3D single-precision slab spreader bins by window origin
+    origin_w = info["w"] if dim == 3 and info["tile3d"] == 2 else 0
+    ref = oracle.binsort(pts, n, m, info["msub"], origin_w=origin_w)
     assert info["nbins"] == ref["counts"].size
     np.testing.assert_array_equal(got["counts"], ref["counts"])
     np.testing.assert_array_equal(got["starts"], ref["starts"])
@@ -119,10 +121,11 @@ def test_setpts_integer_results_match_oracle(dim, N, M, dist, dt, opts):
         np.testing.assert_array_equal(np.sort(got["perm"][lo:lo + cnt]), ref["perm"][lo:lo + cnt])
 
 
-def _boundary_coords(n, rng, count):
+def _boundary_coords(n, rng, count, offset=0.0):
     """float32 coordinates at and next to the floats nearest the cell
-    boundaries 2 pi k / n, one period either side too, in random order."""
-    k = rng.integers(0, n + 1, count).astype(np.float64)
+    boundaries 2 pi (k + offset) / n, one period either side too, in random
+    order."""
+    k = rng.integers(0, n + 1, count).astype(np.float64) + offset
     shift = rng.choice([0.0, -2 * np.pi, 2 * np.pi], count)
     b = (2 * np.pi * k / n + shift).astype(np.float32)
     step = rng.integers(-2, 3, count)
@@ -130,6 +133,35 @@ def _boundary_coords(n, rng, count):
         b = np.where(step >= s, np.nextafter(b, np.float32(np.inf)), b)
         b = np.where(step <= -s, np.nextafter(b, np.float32(-np.inf)), b)
     return b
+
+
+@pytest.mark.parametrize("eps", [1e-6, 1e-5, 1e-7])
+def test_setpts_origins_at_boundaries_match_oracle(eps):
+    """The slab spreader's plans bin points by window origin (ceil(g - w/2)
+    + floor(w/2)): with bins one origin high in y and z, the bin of a point
+    is its y and z origin.  Coordinates at (or next to) the floats nearest
+    the origin boundaries -- half-integer g for odd w (w = 7), integer g for
+    even w (w = 6, 8) -- must get the oracle's double-precision origins."""
+    rng = np.random.default_rng(6)
+    M = 60000
+    N = (20, 24, 18)
+    with nf.Plan(1, N, -1, eps, "complex64", bin2=1) as plan:
+        info0 = plan.info()
+        w = info0["w"]
+        n = [info0["n1"], info0["n2"], info0["n3"]]
+        off = 0.5 if w % 2 else 0.0
+        pts = [rng.uniform(-np.pi, np.pi, M).astype(np.float32),
+               _boundary_coords(n[1], rng, M, off), _boundary_coords(n[2], rng, M, off)]
+        plan.setpts(*[torch.from_numpy(p).to(DEV) for p in pts])
+        info = plan.info()
+        got = plan.sort()
+    assert info["tile3d"] == 2 and info["bin2"] == 1 and info["bin3"] == 1
+    m = [info["bin1"], info["bin2"], info["bin3"]]
+    ref = oracle.binsort(pts, n, m, info["msub"], origin_w=w)
+    np.testing.assert_array_equal(got["counts"], ref["counts"])
+    np.testing.assert_array_equal(got["subproblems"], ref["subproblems"])
+    for lo, cnt in zip(ref["starts"], ref["counts"]):
+        np.testing.assert_array_equal(np.sort(got["perm"][lo:lo + cnt]), ref["perm"][lo:lo + cnt])
 
 
 @pytest.mark.parametrize("N", [(100, 70), (64, 128)])
@@ -186,7 +218,8 @@ def test_regtile_columns_per_lane(cols, dt, eps, rows):
 @pytest.mark.parametrize("eps", [1e-2, 1e-5, 1e-6, 1e-7])
 @pytest.mark.parametrize("N,dist,opts", [((20, 24, 36), "uniform", {}),
                                          ((33, 18, 16), "cluster", {}),
-                                         ((20, 24, 36), "uniform", {"msub": 37, "bin2": 5})])
+                                         ((20, 24, 36), "uniform", {"msub": 37, "bin2": 5}),
+                                         ((20, 24, 36), "wild", {})])
 def test_slab3d_spreader(eps, N, dist, opts):
     """The 3D single-precision spreader with one-cell-thick bins (option
     tile3d = 2; widths 3, 6, 7 and 8 here), ragged grids, clustered points

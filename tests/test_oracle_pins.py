@@ -401,6 +401,36 @@ def test_binsort_handpicked():
     assert r["subproblems"].tolist() == [[0, 0, 2], [0, 2, 1], [1, 3, 1], [5, 4, 2]]
 
 
+def test_binsort_by_window_origin_handpicked():
+    """Binning by window origin: the bin index of a point at fine coordinate g
+    is (ceil(g - w/2) + floor(w/2)) mod n -- for odd w the node nearest g
+    (ties down), for even w the first node at or above g.  Worked by hand on
+    20 x 12 with bins of 8 x 8 (Sec. III-A), w = 7 and w = 6."""
+    n = (20, 12)
+    m = (8, 8)
+    h1, h2 = 2 * np.pi / 20, 2 * np.pi / 12
+    g = [(0.4, 0.6), (7.6, 7.4), (19.7, 11.2), (8.5, 3.0), (15.5, 0.1)]
+    x = [a * h1 for a, _ in g]
+    y = [b * h2 for _, b in g]
+    # w = 7 (odd): index = ceil(g - 3.5) + 3 = ceil(g - 0.5):
+    #   (0.4, 0.6) -> (0, 1); (7.6, 7.4) -> (8, 7); (19.7, 11.2) -> (20 = 0, 11);
+    #   (8.5, 3.0) -> (8, 3) (the tie 8.5 goes down); (15.5, 0.1) -> (15, 0)
+    r = oracle.binsort([x, y], n, m, msub=8, origin_w=7)
+    assert list(r["bin_of"]) == [0, 1, 3, 1, 1]
+    assert list(r["counts"]) == [1, 3, 0, 1, 0, 0]
+    assert list(r["perm"]) == [0, 1, 3, 4, 2]
+    # w = 6 (even): index = ceil(g - 3) + 3 = ceil(g):
+    #   (0.4, 0.6) -> (1, 1); (7.6, 7.4) -> (8, 8); (19.7, 11.2) -> (20 = 0, 12 = 0);
+    #   (8.5, 3.0) -> (9, 3); (15.5, 0.1) -> (16, 1)
+    r = oracle.binsort([x, y], n, m, msub=8, origin_w=6)
+    assert list(r["bin_of"]) == [0, 4, 0, 1, 2]
+    assert list(r["counts"]) == [2, 1, 1, 0, 1, 0]
+    assert list(r["perm"]) == [0, 2, 3, 4, 1]
+    # cell binning of the same points (origin_w = 0) for contrast
+    r = oracle.binsort([x, y], n, m, msub=8)
+    assert list(r["bin_of"]) == [0, 0, 5, 1, 1]
+
+
 def test_binsort_invariants_random():
     rng = np.random.default_rng(3)
     pts = [rng.normal(0, 0.3, 5000) for _ in range(3)]
