@@ -92,7 +92,8 @@ typedef struct nufft_plan_s *nufft_plan_t;
 #define NUFFT_I_TILE3D 15          /* 3D REGTILE spreader in use: 1 planes per warp, 2 slab bins (0: not 3D) */
 #define NUFFT_I_IGROUP 16          /* 3D single-precision SM interpolator: 1 one point per thread,
                                       K >= 2 points of one window origin per thread (0: other) */
-#define NUFFT_I_COUNT 17
+#define NUFFT_I_BIN_ORIGIN 17      /* 1: points binned by window origin (the 3D slab spreader), 0: by cell */
+#define NUFFT_I_COUNT 18
 
 /* Spreading / interpolation methods (option "method"). */
 #define NUFFT_METHOD_AUTO 0
@@ -166,10 +167,13 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *   "tile3d"   3D REGTILE spreader: 1, one block per subproblem, each warp
  *              holding two padded planes of a bin of 32 - 2 ceil(w/2) x 8 x
  *              (16 - 2 ceil(w/2)) cells (16 x 4 x ... in double precision);
- *              2, one warp per subproblem holding all w+1 planes of a bin one
- *              cell thick in z (32 - 2 ceil(w/2) x 32 x 1 cells; complex64 and
- *              w <= 8 only, else BAD_OPT at setpts).  0 (default): 2 where it
- *              applies, else 1.
+ *              2, one warp per subproblem holding the w planes of a bin one
+ *              window origin thick in z (33 - w x 32 x 1 origins; complex64
+ *              and w <= 8 only, else BAD_OPT at setpts).  With 2, setpts bins
+ *              the points by window origin: the bin of a point is that of the
+ *              node ceil(g - w/2) + floor(w/2) (its first support node shifted
+ *              by floor(w/2)) instead of its cell floor(g) (info BIN_ORIGIN).
+ *              0 (default): 2 where it applies, else 1.
  *   "igroup"   3D complex64 SM interpolation: 1, one thread per point; K = 2,
  *              3 or 4, the points of one window origin (the w^3 nodes they
  *              read) in groups of at most K per thread, each tile row loaded
@@ -251,7 +255,9 @@ int nufft_get_info(nufft_plan_t plan, int64_t *info, int n);
 /*
  * Copy the integer results of the last setpts to HOST arrays (for checking
  * the bin sort of Sec. III-A; any argument may be NULL to skip it):
- *   counts[nbins]     points per bin (bins ordered x fastest);
+ *   counts[nbins]     points per bin (bins ordered x fastest; a point's bin is
+ *                     the bin of its cell, or of its window origin node
+ *                     ceil(g - w/2) + floor(w/2) when info BIN_ORIGIN is 1);
  *   starts[nbins]     exclusive prefix sum of counts;
  *   perm[M]           the permutation t: sorted slot -> caller's point index
  *                     (points of bin 0, then bin 1, ...; order inside a bin is

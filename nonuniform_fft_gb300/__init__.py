@@ -31,7 +31,7 @@ ERR_NO_POINTS, ERR_BAD_POINTS, ERR_BAD_OPT, ERR_TOO_LARGE = 6, 7, 8, 9
 METHOD_AUTO, METHOD_SM, METHOD_GM_SORT, METHOD_REGTILE, METHOD_GM = 0, 1, 2, 3, 4
 TIMING_KEYS = ("spread_interp", "fft", "deconv_pad", "zero", "exec", "setpts")
 INFO_KEYS = ("w", "n1", "n2", "n3", "M", "nbins", "nsub", "bin1", "bin2", "bin3", "msub", "method",
-             "batch", "fft", "sms", "tile3d", "igroup")
+             "batch", "fft", "sms", "tile3d", "igroup", "bin_origin")
 
 _lib = None
 

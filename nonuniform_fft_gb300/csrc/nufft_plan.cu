@@ -740,7 +740,8 @@ int nufft_get_info(nufft_plan_t p, int64_t *info, int n) {
   if (!p || !info || n < 0) return NUFFT_ERR_BAD_ARG;
   const int64_t v[NUFFT_I_COUNT] = {p->w,    p->n[0], p->n[1], p->n[2], p->M,      p->nbins,  p->nsub,
                                     p->m[0], p->m[1], p->m[2], p->msub, p->method, batch_pass(p),
-                                    p->fused_fft ? 1 : 0, p->num_sms, p->dim == 3 ? p->tile3d : 0, p->igroup};
+                                    p->fused_fft ? 1 : 0, p->num_sms, p->dim == 3 ? p->tile3d : 0, p->igroup,
+                                    p->bin_origin ? 1 : 0};
   for (int i = 0; i < n && i < NUFFT_I_COUNT; i++) info[i] = v[i];
   return NUFFT_OK;
 }

@@ -111,7 +111,8 @@ def test_setpts_integer_results_match_oracle(dim, N, M, dist, dt, opts):
     n = [info["n1"], info["n2"], info["n3"]][:dim]
     m = [info["bin1"], info["bin2"], info["bin3"]][:dim]
     # the 3D single-precision slab spreader bins by window origin
-    origin_w = info["w"] if dim == 3 and info["tile3d"] == 2 else 0
+    origin_w = info["w"] if info["bin_origin"] else 0
+    assert info["bin_origin"] == (dim == 3 and info["tile3d"] == 2)
     ref = oracle.binsort(pts, n, m, info["msub"], origin_w=origin_w)
     assert info["nbins"] == ref["counts"].size
     np.testing.assert_array_equal(got["counts"], ref["counts"])
@@ -155,7 +156,7 @@ def test_setpts_origins_at_boundaries_match_oracle(eps):
         plan.setpts(*[torch.from_numpy(p).to(DEV) for p in pts])
         info = plan.info()
         got = plan.sort()
-    assert info["tile3d"] == 2 and info["bin2"] == 1 and info["bin3"] == 1
+    assert info["tile3d"] == 2 and info["bin_origin"] == 1 and info["bin2"] == 1 and info["bin3"] == 1
     m = [info["bin1"], info["bin2"], info["bin3"]]
     ref = oracle.binsort(pts, n, m, info["msub"], origin_w=w)
     np.testing.assert_array_equal(got["counts"], ref["counts"])
