@@ -318,7 +318,7 @@ def kernel_names(wl: W.Workload, method1: int, method2: int, tile3d: int = 1, ig
                3: "spread_slab3d_kernel" if tile3d == 2 else "spread_plane3d" + df + "_kernel"}[wl.dim]
     spread = {nf.METHOD_SM: "spread_sm_kernel", nf.METHOD_GM_SORT: "spread_gm_kernel",
               nf.METHOD_GM: "spread_gmu_kernel", nf.METHOD_REGTILE: regtile}[method1]
-    sm_interp = {1: "interp_sm1d_kernel", 2: "interp_sm_kernel",
+    sm_interp = {1: "interp_sm1d" + df + "_kernel", 2: "interp_sm_kernel",
                  3: "interp_sm3d_df_kernel" if wl.dtype == "f64" else
                  ("interp_group3d_kernel" if igroup >= 2 else "interp_sm3d_bank_kernel")}
     interp = {nf.METHOD_GM_SORT: "interp_gm_kernel", nf.METHOD_GM: "interp_gmu_kernel"}.get(
