@@ -184,7 +184,7 @@ int nufft_makeplan_upsampled(int type, int dim, const int64_t *n_modes, int ifla
  *              BAD_OPT at setpts).  0 (default): 2 where it applies, else 1.
  *              Other plans ignore it.
  *   "fft"      0 (default): 2D complex64 plans whose fine grid sizes are
- *              powers of two from 256 to 4096 take the fine-grid FFT as two
+ *              powers of two from 128 to 4096 take the fine-grid FFT as two
  *              passes of the library's own kernels, pruned to the modes of
  *              I_N and fused with the correction of eq. (10) / (11); other
  *              plans use cuFFT.  1: always cuFFT and the separate correction

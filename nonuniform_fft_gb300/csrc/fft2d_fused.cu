@@ -19,7 +19,7 @@
 // instead of several times.
 //
 // Each transform is a radix-8 Stockham FFT (the last radix 4 or 2) of
-// L = 2^a complex values, 256 <= L <= 4096, in shared memory.  Stage s with
+// L = 2^a complex values, 128 <= L <= 4096, in shared memory.  Stage s with
 // stride Ns (product of the earlier radices) takes, for butterfly j, the R
 // values at j + r L/R, multiplies value r by w^{(j mod Ns) r L/(Ns R)}
 // (w = exp(s 2 pi i / L), s the plan's sign), takes their R-point DFT and
@@ -40,7 +40,7 @@
 namespace nufft {
 namespace {
 
-constexpr int kMinLog = 8;        // L = 256
+constexpr int kMinLog = 7;        // L = 128
 constexpr int kMaxLog = 12;       // L = 4096
 
 __host__ __device__ constexpr int padded(int i) { return i + (i >> 4); }
@@ -334,6 +334,7 @@ cudaError_t launch_pass(Pass pass, const FusedArgs &a, int nvec, cudaStream_t st
 template <int S>
 cudaError_t launch_len(int L, Pass pass, const FusedArgs &a, int nvec, cudaStream_t st) {
   switch (L) {
+    case 128: return launch_pass<128, S>(pass, a, nvec, st);
     case 256: return launch_pass<256, S>(pass, a, nvec, st);
     case 512: return launch_pass<512, S>(pass, a, nvec, st);
     case 1024: return launch_pass<1024, S>(pass, a, nvec, st);

@@ -23,8 +23,8 @@ DEV = torch.device("cuda:0")
 
 # N -> fine grid n = smallest 2^a 3^b 5^c >= 2 N: (128, 128) -> (256, 256);
 # odd (127, 255) -> (256, 512); (1024, 128) -> (2048, 256);
-# (2048, 128) -> (4096, 256)
-SIZES = [(128, 128), (127, 255), (1024, 128), (2048, 128)]
+# (2048, 128) -> (4096, 256); (64, 64) -> (128, 128); (64, 1024) -> (128, 2048)
+SIZES = [(128, 128), (127, 255), (1024, 128), (2048, 128), (64, 64), (64, 1024)]
 
 
 def _pts(M, rng):
@@ -126,7 +126,7 @@ def test_fused_not_used_where_unsupported():
     rng = np.random.default_rng(65)
     pts = _pts(1000, rng)
     c = _cplx(1000, rng)
-    for N in [(100, 70), (64, 64)]:   # fine grids 200 x 140 (not 2^a) and 128 x 128 (below 256)
+    for N in [(100, 70), (32, 32)]:   # fine grids 200 x 140 (not 2^a) and 64 x 64 (below 128)
         _, info = _run(1, N, pts, c, 1e-5, -1)
         assert info["fft"] == 0
     xs = [torch.from_numpy(p.astype(np.float64)).to(DEV) for p in pts]
